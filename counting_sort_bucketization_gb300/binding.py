@@ -1,0 +1,267 @@
+"""Python binding of libmoe_layout.so (include/moe_layout.h), via ctypes.
+
+Argument marshalling only: each function checks that the torch tensors it is
+given have the dtype, device and layout the C ABI expects, passes their data
+pointers and the current CUDA stream, and raises ``LayoutError`` on a
+non-zero status.  Every step of the computation runs in the library's CUDA
+kernels; there is no fallback.  If the library has not been built, the first
+call raises.
+
+A description (``desc``) is any object with the attributes ``num_tokens``,
+``topk``, ``num_experts``, ``num_ranks`` and ``alignment`` (for instance a
+``workloads.Workload``, or ``LayoutDesc``).
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+ERROR_NAMES = {
+    0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_CUDA", 3: "MOE_ERR_BAD_EXPERT_ID",
+    4: "MOE_ERR_CAPACITY", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_UNSUPPORTED",
+}
+
+
+class LayoutError(RuntimeError):
+    def __init__(self, what: str, status: int):
+        super().__init__(f"{what}: {ERROR_NAMES.get(status, status)} ({strerror(status)})")
+        self.status = status
+
+
+@dataclasses.dataclass(frozen=True)
+class LayoutDesc:
+    num_tokens: int
+    topk: int
+    num_experts: int
+    num_ranks: int
+    alignment: int
+
+
+class _CDesc(ctypes.Structure):
+    _fields_ = [("num_tokens", ctypes.c_int64), ("topk", ctypes.c_int32), ("num_experts", ctypes.c_int32),
+                ("num_ranks", ctypes.c_int32), ("alignment", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib: ctypes.CDLL | None = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library() -> ctypes.CDLL:
+    """Open libmoe_layout.so (built by ``build.build()``); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is not built: run counting_sort_bucketization_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        p, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        dp = ctypes.POINTER(_CDesc)
+        lib.moe_layout_workspace_bytes.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t)]
+        lib.moe_layout_count.argtypes = [dp, p, p, p, p, sz, p]
+        lib.moe_layout_scan.argtypes = [dp, p, p, p, p, sz, p, p, p, p, i64, p, p]
+        lib.moe_dispatch_permute.argtypes = [dp, p, i64, p, i64, p, p, p, p, p, i64, ctypes.c_int, p, sz, p]
+        lib.moe_combine_unpermute.argtypes = [dp, p, i64, i64, p, p, p, p, sz, p]
+        lib.moe_layout_get_error.argtypes = [p, ctypes.POINTER(i32), p]
+        lib.moe_strerror.argtypes = [ctypes.c_int]
+        lib.moe_strerror.restype = ctypes.c_char_p
+        lib.moe_kernel_launches.argtypes = []
+        lib.moe_kernel_launches.restype = ctypes.c_uint64
+        for name in ("moe_layout_workspace_bytes", "moe_layout_count", "moe_layout_scan",
+                     "moe_dispatch_permute", "moe_combine_unpermute", "moe_layout_get_error"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def strerror(status: int) -> str:
+    return load_library().moe_strerror(int(status)).decode()
+
+
+def kernel_launches() -> int:
+    """Kernels the library has launched in this process."""
+    return int(load_library().moe_kernel_launches())
+
+
+def _desc(d) -> _CDesc:
+    return _CDesc(int(d.num_tokens), int(d.topk), int(d.num_experts), int(d.num_ranks), int(d.alignment))
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise LayoutError(what, status)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor | None, name: str, dtype=None, numel=None, allow_none=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} needs at least {numel} elements, has {t.numel()}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def workspace_bytes(desc) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().moe_layout_workspace_bytes(ctypes.byref(_desc(desc)), ctypes.byref(n)),
+           "moe_layout_workspace_bytes")
+    return int(n.value)
+
+
+def new_workspace(desc, device="cuda") -> torch.Tensor:
+    """Zero-filled workspace for ``desc`` (torch's allocations are 256-byte aligned)."""
+    return torch.zeros(max(workspace_bytes(desc), 256), dtype=torch.uint8, device=device)
+
+
+def layout_count(desc, topk_idx, expert_count, rank_count, workspace, stream=None) -> None:
+    N, K, E, R = int(desc.num_tokens), int(desc.topk), int(desc.num_experts), int(desc.num_ranks)
+    st = load_library().moe_layout_count(
+        ctypes.byref(_desc(desc)), _dev(topk_idx, "topk_idx", torch.int64, N * K),
+        _dev(expert_count, "expert_count", torch.int32, E), _dev(rank_count, "rank_count", torch.int32, R),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    _check(st, "moe_layout_count")
+
+
+def layout_scan(desc, topk_idx, expert_count, rank_count, workspace, expert_offset, rank_psum, dst_slot,
+                src_idx, total_rows, stream=None) -> None:
+    N, K, E, R = int(desc.num_tokens), int(desc.topk), int(desc.num_experts), int(desc.num_ranks)
+    st = load_library().moe_layout_scan(
+        ctypes.byref(_desc(desc)), _dev(topk_idx, "topk_idx", torch.int64, N * K),
+        _dev(expert_count, "expert_count", torch.int32, E), _dev(rank_count, "rank_count", torch.int32, R),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+        _dev(expert_offset, "expert_offset", torch.int32, E + 1), _dev(rank_psum, "rank_psum", torch.int32, R),
+        _dev(dst_slot, "dst_slot", torch.int32, N * K), _dev(src_idx, "src_idx", torch.int32),
+        src_idx.numel(), _dev(total_rows, "total_rows", torch.int32, 1), _stream(stream))
+    _check(st, "moe_layout_scan")
+
+
+def _row_bytes(t: torch.Tensor, rows: int) -> int:
+    if rows == 0:
+        return t.shape[-1] * t.element_size() if t.dim() >= 2 else 0
+    return t.numel() * t.element_size() // rows
+
+
+def dispatch_permute(desc, x, dst_slot, expert_offset, expert_count, recv_x, workspace, sf=None,
+                     recv_sf=None, zero_pad=True, stream=None) -> None:
+    """recv_x[dst_slot[t,k]] = x[t] (bytes); gap rows zeroed.  x [N, ...], recv_x [capacity, ...]."""
+    N, K, E = int(desc.num_tokens), int(desc.topk), int(desc.num_experts)
+    cap = recv_x.shape[0]
+    rb = x.shape[1] * x.element_size() if x.dim() == 2 else _row_bytes(x, N)
+    if recv_x.numel() * recv_x.element_size() != cap * rb:
+        raise ValueError("recv_x rows must have the same byte size as x rows")
+    srb = 0
+    if sf is not None:
+        srb = sf.shape[1] * sf.element_size()
+        if recv_sf is None or recv_sf.shape[0] != cap or recv_sf.numel() * recv_sf.element_size() != cap * srb:
+            raise ValueError("recv_sf must be [capacity, sf row] when sf is given")
+    st = load_library().moe_dispatch_permute(
+        ctypes.byref(_desc(desc)), _dev(x, "x"), rb, _dev(sf, "sf", allow_none=True), srb,
+        _dev(dst_slot, "dst_slot", torch.int32, N * K), _dev(expert_offset, "expert_offset", torch.int32, E + 1),
+        _dev(expert_count, "expert_count", torch.int32, E), _dev(recv_x, "recv_x"),
+        _dev(recv_sf, "recv_sf", allow_none=True), cap, 1 if zero_pad else 0,
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    _check(st, "moe_dispatch_permute")
+
+
+def combine_unpermute(desc, expert_out, dst_slot, weights, out, workspace, stream=None) -> None:
+    """out[t] = bf16(sum_k w[t,k] * expert_out[dst_slot[t,k]]) with an fp32 fma chain."""
+    N, K = int(desc.num_tokens), int(desc.topk)
+    if expert_out.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
+        raise ValueError("expert_out and out must be bfloat16")
+    H = expert_out.shape[1]
+    if out.shape != (N, H):
+        raise ValueError(f"out must be [{N}, {H}]")
+    st = load_library().moe_combine_unpermute(
+        ctypes.byref(_desc(desc)), _dev(expert_out, "expert_out"), expert_out.shape[0], H,
+        _dev(dst_slot, "dst_slot", torch.int32, N * K), _dev(weights, "weights", torch.float32, N * K),
+        _dev(out, "out"), _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    _check(st, "moe_combine_unpermute")
+
+
+def get_error(workspace, stream=None) -> int:
+    """Synchronise, read and clear the workspace's sticky device error (0 = none)."""
+    v = ctypes.c_int32(0)
+    _check(load_library().moe_layout_get_error(_dev(workspace, "workspace", torch.uint8), ctypes.byref(v),
+                                               _stream(stream)), "moe_layout_get_error")
+    return int(v.value)
+
+
+class Layout:
+    """Device buffers of one dispatch layout (counts, offsets, maps) plus its workspace."""
+
+    def __init__(self, desc, capacity_rows: int, device="cuda"):
+        self.desc = desc
+        self.capacity = int(capacity_rows)
+        N, K, E, R = int(desc.num_tokens), int(desc.topk), int(desc.num_experts), int(desc.num_ranks)
+        i32 = dict(dtype=torch.int32, device=device)
+        self.workspace = new_workspace(desc, device)
+        self.expert_count = torch.zeros(E, **i32)
+        self.rank_count = torch.zeros(R, **i32)
+        self.expert_offset = torch.zeros(E + 1, **i32)
+        self.rank_psum = torch.zeros(R, **i32)
+        self.dst_slot = torch.empty(max(N * K, 1), **i32)
+        self.src_idx = torch.empty(max(self.capacity, 1), **i32)[: self.capacity]
+        self.total_rows = torch.zeros(1, **i32)
+
+    def count(self, topk_idx, stream=None):
+        layout_count(self.desc, topk_idx, self.expert_count, self.rank_count, self.workspace, stream)
+
+    def scan(self, topk_idx, stream=None):
+        layout_scan(self.desc, topk_idx, self.expert_count, self.rank_count, self.workspace, self.expert_offset,
+                    self.rank_psum, self.dst_slot, self.src_idx, self.total_rows, stream)
+
+    def build(self, topk_idx, stream=None):
+        self.count(topk_idx, stream)
+        self.scan(topk_idx, stream)
+        return self
+
+    def permute(self, x, recv_x, sf=None, recv_sf=None, zero_pad=True, stream=None):
+        dispatch_permute(self.desc, x, self.dst_slot, self.expert_offset, self.expert_count, recv_x,
+                         self.workspace, sf, recv_sf, zero_pad, stream)
+
+    def combine(self, expert_out, weights, out, stream=None):
+        combine_unpermute(self.desc, expert_out, self.dst_slot, weights, out, self.workspace, stream)
+
+    def error(self, stream=None) -> int:
+        return get_error(self.workspace, stream)
+
+
+def dispatch(topk_idx, x, num_experts, num_ranks, alignment, sf=None, capacity_rows=None, stream=None):
+    """Count, scan and permute in one call; returns ``(layout, recv_x, recv_sf)``.
+
+    With ``capacity_rows`` None the receive buffers get the bound that never
+    overflows (N*K + E*(A-1) rows), so no host synchronisation is needed.
+    """
+    N, K = topk_idx.shape
+    desc = LayoutDesc(N, K, num_experts, num_ranks, alignment)
+    cap = capacity_rows if capacity_rows is not None else N * K + num_experts * (alignment - 1)
+    lay = Layout(desc, cap, device=topk_idx.device).build(topk_idx, stream)
+    recv_x = torch.empty((cap,) + tuple(x.shape[1:]), dtype=x.dtype, device=x.device)
+    recv_sf = None
+    if sf is not None:
+        recv_sf = torch.empty((cap,) + tuple(sf.shape[1:]), dtype=sf.dtype, device=sf.device)
+    lay.permute(x, recv_x, sf, recv_sf, stream=stream)
+    return lay, recv_x, recv_sf

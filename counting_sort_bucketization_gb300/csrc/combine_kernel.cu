@@ -1,0 +1,116 @@
+// combine_kernel.cu -- inverse of the dispatch on sm_103a: gather each
+// token's expert-output rows through dst_slot and reduce them with the
+// token's top-k weights.
+//
+//   out[t, h] = bf16_rn( fma(w[t,K-1], y[K-1], ... fma(w[t,0], y[0], 0.0f)) )
+//   with y[k] = float(expert_out[dst_slot[t,k], h]), masked k skipped.
+//
+// The page "07 DeepEP Counting Sort / Bucketization" keeps the slot map for
+// the combine (§6.2) but prints no combine arithmetic; the order above (fp32
+// from 0, ascending k, one fused multiply-add per term, one bf16 rounding) is
+// the plain definition and makes the result bit-reproducible.
+//
+// HBM-bound: each thread owns 16-byte column vectors of the row and issues
+// the loads of up to 8 expert rows before any arithmetic, so 8 x 16 B per
+// thread are in flight; slots and weights of the CTA's token block are staged
+// in shared memory once.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kCombineThreads = 256;
+constexpr int kKGroup = 8;              // expert rows loaded before their FMAs
+constexpr int kMaxTokensPerCta = 64;
+
+__device__ __forceinline__ void fma_bf16x8(float (&acc)[8], float w, const uint4& v) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc[2 * i] = __fmaf_rn(w, __uint_as_float(u[i] << 16), acc[2 * i]);
+    acc[2 * i + 1] = __fmaf_rn(w, __uint_as_float(u[i] & 0xffff0000u), acc[2 * i + 1]);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_kernel(const CombineArgs a, int tokens_per_cta) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int K = a.topk;
+  int32_t* slot_s = reinterpret_cast<int32_t*>(smem);
+  float* w_s = reinterpret_cast<float*>(smem + sizeof(int32_t) * tokens_per_cta * K);
+
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * tokens_per_cta;
+  const int ntok = static_cast<int>(max64(0, min64(tokens_per_cta, a.num_tokens - t0)));
+  for (int i = threadIdx.x; i < ntok * K; i += kCombineThreads) {
+    int s = __ldg(a.dst_slot + t0 * K + i);
+    if (s >= a.expert_out_rows) {
+      set_error(a.err, MOE_ERR_CAPACITY);
+      s = -1;
+    }
+    slot_s[i] = s;
+    w_s[i] = __ldg(a.weights + t0 * K + i);
+  }
+  __syncthreads();
+
+  const int64_t H = a.hidden;
+  const int nvec = static_cast<int>(H / 8);
+  for (int tt = 0; tt < ntok; ++tt) {
+    const int32_t* sl = slot_s + tt * K;
+    const float* wt = w_s + tt * K;
+    uint16_t* orow = a.out + (t0 + tt) * H;
+    for (int j = threadIdx.x; j < nvec; j += kCombineThreads) {
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+      for (int kg = 0; kg < K; kg += kKGroup) {
+        uint4 v[kKGroup];
+#pragma unroll
+        for (int q = 0; q < kKGroup; ++q) {
+          const int k = kg + q;
+          const int32_t s = k < K ? sl[k] : -1;
+          v[q] = s >= 0 ? ptx::ld_nc_v4(a.expert_out + static_cast<int64_t>(s) * H + j * 8)
+                        : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int q = 0; q < kKGroup; ++q) {
+          const int k = kg + q;
+          if (k < K && sl[k] >= 0) fma_bf16x8(acc, wt[k], v[q]);
+        }
+      }
+      uint4 o;
+      o.x = pack_bf16x2(acc[0], acc[1]);
+      o.y = pack_bf16x2(acc[2], acc[3]);
+      o.z = pack_bf16x2(acc[4], acc[5]);
+      o.w = pack_bf16x2(acc[6], acc[7]);
+      ptx::st_v4(orow + j * 8, o);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
+  const int sms = device_sm_count();
+  const int64_t target_ctas = 4ll * sms;
+  int64_t tpc = ceil_div64(max64(a.num_tokens, 1), target_ctas);
+  tpc = max64(1, min64(tpc, kMaxTokensPerCta));
+  const int64_t grid = max64(1, ceil_div64(a.num_tokens, tpc));
+  const size_t smem = (sizeof(int32_t) + sizeof(float)) * static_cast<size_t>(tpc) * a.topk;
+  combine_kernel<<<static_cast<unsigned>(grid), kCombineThreads, smem, stream>>>(a, static_cast<int>(tpc));
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,77 @@
+// common.cuh -- definitions shared by the library's kernels and its C-ABI
+// host code: the tile plan of the count / rank kernels, the workspace layout,
+// the sticky device error word and the kernel-launch counter.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/moe_layout.h"
+
+namespace moe {
+
+constexpr int kWarpSize = 32;
+constexpr int kLayoutWarps = 8;                        // warps per count / rank CTA
+constexpr int kLayoutThreads = kLayoutWarps * kWarpSize;
+constexpr int kMaxChunksPerWarp = 16;
+constexpr int kTargetTiles = 256;                      // tiles the plan aims for
+constexpr uint64_t kWaitLimitNs = 1000000000ull;       // 1 s bound on any in-kernel wait
+
+// The count and rank kernels walk topk_idx in token-aligned chunks of one warp:
+// a chunk holds tpc = 32 / K whole tokens (tpc * K <= 32 lanes busy), a warp
+// walks cpw consecutive chunks and a CTA (tile) holds kLayoutWarps warps.
+// Pairs (t, k) of a tile are contiguous in topk_idx, so a tile's pairs in
+// (warp, chunk, lane) order are exactly its pairs in (t, k) order.
+struct TilePlan {
+  int tpc;           // tokens per chunk
+  int lanes;         // busy lanes per chunk = tpc * K
+  int cpw;           // chunks per warp
+  int tile_tokens;   // tokens per tile = kLayoutWarps * cpw * tpc
+  int64_t tiles;     // T = ceil(N / tile_tokens)
+};
+
+__host__ __device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+__host__ __device__ inline int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ inline int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+
+inline TilePlan make_tile_plan(int64_t N, int K) {
+  TilePlan p;
+  p.tpc = kWarpSize / K;
+  p.lanes = p.tpc * K;
+  const int64_t per_cpw = static_cast<int64_t>(kLayoutWarps) * p.tpc;
+  int64_t cpw = ceil_div64(N, per_cpw * kTargetTiles);
+  if (cpw < 1) cpw = 1;
+  if (cpw > kMaxChunksPerWarp) cpw = kMaxChunksPerWarp;
+  p.cpw = static_cast<int>(cpw);
+  p.tile_tokens = static_cast<int>(per_cpw * cpw);
+  p.tiles = ceil_div64(N, p.tile_tokens);
+  return p;
+}
+
+// Workspace: [error word | pad to 256 B][hist int32 E x T][rank hist int32 R x T]
+// hist[e][tile] is expert e's count in the tile; the column scan turns it
+// into the count of expert e in all earlier tiles.
+struct WorkspaceLayout {
+  size_t err_off = 0;
+  size_t hist_off = 256;
+  size_t rhist_off = 0;
+  size_t bytes = 0;
+};
+
+inline WorkspaceLayout make_workspace_layout(const moe_layout_desc& d, const TilePlan& p) {
+  WorkspaceLayout w;
+  const size_t T = static_cast<size_t>(p.tiles);
+  w.rhist_off = w.hist_off + ((static_cast<size_t>(d.num_experts) * T * 4 + 255) / 256) * 256;
+  w.bytes = w.rhist_off + ((static_cast<size_t>(d.num_ranks) * T * 4 + 255) / 256) * 256;
+  return w;
+}
+
+// First error wins; later ones are dropped.
+__device__ __forceinline__ void set_error(int* err, int code) { atomicCAS(err, 0, code); }
+
+// Counter behind moe_kernel_launches().
+void count_launch(int n = 1);
+
+}  // namespace moe

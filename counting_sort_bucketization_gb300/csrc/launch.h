@@ -1,0 +1,64 @@
+// launch.h -- host-side launchers of the library's kernels (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace moe {
+
+size_t count_smem_bytes(const moe_layout_desc& d, const TilePlan& p);
+size_t rank_smem_bytes(const moe_layout_desc& d, const TilePlan& p);
+
+// count_tiles_kernel + scan_columns_kernel.
+cudaError_t launch_count(const moe_layout_desc& d, const TilePlan& p, const int64_t* topk_idx,
+                         int32_t* expert_count, int32_t* rank_count, int* err, int32_t* hist,
+                         int32_t* rhist, cudaStream_t stream);
+
+// rank_maps_kernel.
+cudaError_t launch_rank(const moe_layout_desc& d, const TilePlan& p, const int64_t* topk_idx,
+                        const int32_t* hist_prefix, const int32_t* expert_count,
+                        const int32_t* rank_count, int32_t* expert_offset, int32_t* rank_psum,
+                        int32_t* dst_slot, int32_t* src_idx, int64_t capacity,
+                        int32_t* total_rows, int* err, cudaStream_t stream);
+
+struct PermuteArgs {
+  const uint8_t* x;
+  const uint8_t* sf;
+  int64_t row_bytes;
+  int64_t sf_row_bytes;
+  const int32_t* dst_slot;
+  const int32_t* expert_offset;
+  const int32_t* expert_count;
+  uint8_t* recv_x;
+  uint8_t* recv_sf;
+  int64_t capacity;
+  int64_t num_tokens;
+  int topk;
+  int num_experts;
+  int zero_pad;
+  int* err;
+};
+
+cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t stream);
+
+struct CombineArgs {
+  const uint16_t* expert_out;  // bf16 bits
+  int64_t expert_out_rows;
+  int64_t hidden;
+  const int32_t* dst_slot;
+  const float* weights;
+  uint16_t* out;               // bf16 bits
+  int64_t num_tokens;
+  int topk;
+  int* err;
+};
+
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
+
+// Streaming multiprocessors of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace moe

@@ -1,0 +1,201 @@
+// moe_layout_api.cu -- the extern "C" entry points of libmoe_layout.so:
+// argument checks, workspace carving and kernel launches.  Semantics and
+// error behaviour of each call are documented in include/moe_layout.h.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+
+static std::atomic<uint64_t> g_launches{0};
+
+void count_launch(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
+
+int device_sm_count() {
+  static std::mutex mu;
+  static std::vector<int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= static_cast<int>(cache.size())) cache.resize(dev + 1, 0);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_desc(const moe_layout_desc* d) {
+  if (d == nullptr) return MOE_ERR_INVALID_ARG;
+  if (d->num_tokens < 0 || d->topk < 1 || d->num_experts < 1 || d->num_ranks < 1 || d->alignment < 1)
+    return MOE_ERR_INVALID_ARG;
+  if (d->num_experts % d->num_ranks != 0) return MOE_ERR_INVALID_ARG;
+  if (d->topk > MOE_MAX_TOPK || d->num_experts > MOE_MAX_EXPERTS) return MOE_ERR_UNSUPPORTED;
+  // Every slot and row index must fit int32.
+  const int64_t worst = d->num_tokens * d->topk + static_cast<int64_t>(d->num_experts) * (d->alignment - 1);
+  if (d->num_tokens > (int64_t{1} << 31) / d->topk || worst >= (int64_t{1} << 31))
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int check_workspace(const moe_layout_desc* d, const void* ws, size_t ws_bytes, WorkspaceLayout* out) {
+  const WorkspaceLayout w = make_workspace_layout(*d, make_tile_plan(d->num_tokens, d->topk));
+  if (ws == nullptr || !aligned(ws, 256) || ws_bytes < w.bytes) return MOE_ERR_INVALID_ARG;
+  *out = w;
+  return MOE_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_layout_workspace_bytes(const moe_layout_desc* desc, size_t* bytes) {
+  if (int st = check_desc(desc)) return st;
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  *bytes = make_workspace_layout(*desc, make_tile_plan(desc->num_tokens, desc->topk)).bytes;
+  return MOE_OK;
+}
+
+int moe_layout_count(const moe_layout_desc* desc, const int64_t* topk_idx, int32_t* expert_count,
+                     int32_t* rank_count, void* workspace, size_t workspace_bytes, void* stream) {
+  if (int st = check_desc(desc)) return st;
+  WorkspaceLayout w;
+  if (int st = check_workspace(desc, workspace, workspace_bytes, &w)) return st;
+  if ((desc->num_tokens > 0 && topk_idx == nullptr) || expert_count == nullptr || rank_count == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  const TilePlan p = make_tile_plan(desc->num_tokens, desc->topk);
+  return cuda_status(launch_count(*desc, p, topk_idx, expert_count, rank_count, at<int>(workspace, w.err_off),
+                                  at<int32_t>(workspace, w.hist_off), at<int32_t>(workspace, w.rhist_off),
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+int moe_layout_scan(const moe_layout_desc* desc, const int64_t* topk_idx, const int32_t* expert_count,
+                    const int32_t* rank_count, void* workspace, size_t workspace_bytes,
+                    int32_t* expert_offset, int32_t* rank_psum, int32_t* dst_slot, int32_t* src_idx,
+                    int64_t capacity_rows, int32_t* total_rows, void* stream) {
+  if (int st = check_desc(desc)) return st;
+  WorkspaceLayout w;
+  if (int st = check_workspace(desc, workspace, workspace_bytes, &w)) return st;
+  const bool has_pairs = desc->num_tokens > 0;
+  if ((has_pairs && (topk_idx == nullptr || dst_slot == nullptr)) || expert_count == nullptr ||
+      rank_count == nullptr || expert_offset == nullptr || rank_psum == nullptr || total_rows == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (capacity_rows < 0 || (capacity_rows > 0 && src_idx == nullptr)) return MOE_ERR_INVALID_ARG;
+  const TilePlan p = make_tile_plan(desc->num_tokens, desc->topk);
+  return cuda_status(launch_rank(*desc, p, topk_idx, at<int32_t>(workspace, w.hist_off), expert_count,
+                                 rank_count, expert_offset, rank_psum, dst_slot, src_idx, capacity_rows,
+                                 total_rows, at<int>(workspace, w.err_off), static_cast<cudaStream_t>(stream)));
+}
+
+int moe_dispatch_permute(const moe_layout_desc* desc, const void* x, int64_t row_bytes, const void* sf,
+                         int64_t sf_row_bytes, const int32_t* dst_slot, const int32_t* expert_offset,
+                         const int32_t* expert_count, void* recv_x, void* recv_sf, int64_t capacity_rows,
+                         int zero_pad, void* workspace, size_t workspace_bytes, void* stream) {
+  if (int st = check_desc(desc)) return st;
+  WorkspaceLayout w;
+  if (int st = check_workspace(desc, workspace, workspace_bytes, &w)) return st;
+  const bool has_pairs = desc->num_tokens > 0;
+  if (row_bytes <= 0 || row_bytes % 16 != 0 || capacity_rows < 0) return MOE_ERR_INVALID_ARG;
+  if ((has_pairs && (x == nullptr || dst_slot == nullptr)) || expert_offset == nullptr ||
+      expert_count == nullptr || (capacity_rows > 0 && recv_x == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(recv_x, 16)) return MOE_ERR_INVALID_ARG;
+  if (sf != nullptr) {
+    if (sf_row_bytes <= 0 || sf_row_bytes % 4 != 0 || !aligned(sf, 4) || !aligned(recv_sf, 4) ||
+        (capacity_rows > 0 && recv_sf == nullptr))
+      return MOE_ERR_INVALID_ARG;
+  }
+  PermuteArgs a{};
+  a.x = static_cast<const uint8_t*>(x);
+  a.sf = static_cast<const uint8_t*>(sf);
+  a.row_bytes = row_bytes;
+  a.sf_row_bytes = sf != nullptr ? sf_row_bytes : 0;
+  a.dst_slot = dst_slot;
+  a.expert_offset = expert_offset;
+  a.expert_count = expert_count;
+  a.recv_x = static_cast<uint8_t*>(recv_x);
+  a.recv_sf = sf != nullptr ? static_cast<uint8_t*>(recv_sf) : nullptr;
+  a.capacity = capacity_rows;
+  a.num_tokens = desc->num_tokens;
+  a.topk = desc->topk;
+  a.num_experts = desc->num_experts;
+  a.zero_pad = zero_pad != 0;
+  a.err = at<int>(workspace, w.err_off);
+  return cuda_status(launch_permute(a, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_combine_unpermute(const moe_layout_desc* desc, const void* expert_out, int64_t expert_out_rows,
+                          int64_t hidden, const int32_t* dst_slot, const float* weights, void* out,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  if (int st = check_desc(desc)) return st;
+  WorkspaceLayout w;
+  if (int st = check_workspace(desc, workspace, workspace_bytes, &w)) return st;
+  if (hidden <= 0 || hidden % 8 != 0 || expert_out_rows < 0) return MOE_ERR_INVALID_ARG;
+  if (desc->num_tokens == 0) return MOE_OK;
+  if (dst_slot == nullptr || weights == nullptr || out == nullptr ||
+      (expert_out_rows > 0 && expert_out == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(expert_out, 16) || !aligned(out, 16) || !aligned(weights, 4)) return MOE_ERR_INVALID_ARG;
+  CombineArgs a{};
+  a.expert_out = static_cast<const uint16_t*>(expert_out);
+  a.expert_out_rows = expert_out_rows;
+  a.hidden = hidden;
+  a.dst_slot = dst_slot;
+  a.weights = weights;
+  a.out = static_cast<uint16_t*>(out);
+  a.num_tokens = desc->num_tokens;
+  a.topk = desc->topk;
+  a.err = at<int>(workspace, w.err_off);
+  return cuda_status(launch_combine(a, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_layout_get_error(void* workspace, int32_t* device_error, void* stream) {
+  if (workspace == nullptr || device_error == nullptr) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t host = 0;
+  cudaError_t e = cudaMemcpyAsync(&host, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  *device_error = host;
+  return MOE_OK;
+}
+
+const char* moe_strerror(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_BAD_EXPERT_ID: return "expert id >= num_experts";
+    case MOE_ERR_CAPACITY: return "receive buffer capacity exceeded";
+    case MOE_ERR_TIMEOUT: return "bounded wait in a kernel timed out";
+    case MOE_ERR_UNSUPPORTED: return "sizes beyond this build's limits";
+    default: return "unknown status";
+  }
+}
+
+uint64_t moe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

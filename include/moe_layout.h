@@ -1,0 +1,180 @@
+/*
+ * moe_layout.h -- C ABI of the GB300 MoE dispatch-layout library
+ * (libmoe_layout.so): token dispatch as a counting sort / bucketization,
+ * and its inverse combine, on one GPU.
+ *
+ * The method is the one described on the page
+ *   "07 DeepEP Counting Sort / Bucketization 深度校验：博客第一性原理 vs 源码实现"
+ * cited as [CS] with its section numbers: count tokens per expert and per
+ * logical rank (§4.2), prefix-sum the aligned counts (§5.2-§5.5, §7.2),
+ * scatter every (token, expert) copy of a row into an expert-major buffer
+ * (§6.4, §8.2) with zero rows in the alignment gaps (§7.3).  Combine is the
+ * inverse gather with a top-k weighted sum.
+ *
+ * Conventions shared by every entry point
+ *  - All array pointers are DEVICE pointers owned by the caller.  The library
+ *    allocates no memory; scratch lives in a caller-provided workspace whose
+ *    size moe_layout_workspace_bytes() returns.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL means the
+ *    legacy default stream) and returns before the GPU work finishes, except
+ *    moe_layout_get_error(), which synchronises the stream.
+ *  - Return value: MOE_OK, or an error found on the host before anything was
+ *    launched (MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED), or MOE_ERR_CUDA if a
+ *    launch failed.  Errors found by the kernels (bad expert id, capacity,
+ *    timeout) are recorded in the workspace's sticky error word and read
+ *    with moe_layout_get_error().
+ *  - Notation: N tokens, K top-k slots, E experts, R logical ranks,
+ *    L = E / R experts per rank, A alignment.  Logical rank r owns experts
+ *    [r*L, (r+1)*L); ranks are partitions of one GPU buffer, not devices.
+ *  - topk_idx is int64 [N, K] row-major; a negative entry is a masked slot;
+ *    an entry >= E is an error (MOE_ERR_BAD_EXPERT_ID) and the slot is then
+ *    treated as masked.
+ *  - Slots and row indices are int32: N*K + E*(A-1) must be < 2^31.
+ *  - Results are deterministic: the slot of a (token, k) pair inside its
+ *    expert's segment is its rank in (token, k) order among that expert's
+ *    pairs, independent of scheduling.  ([CS] §6.2/§6.4 hand out slots with
+ *    atomics instead, so their order varies from run to run.)
+ *
+ * Kernels are compiled for sm_103a only.
+ */
+#ifndef MOE_LAYOUT_H_
+#define MOE_LAYOUT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes.  0 is success. */
+enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* host check failed: null pointer, bad size or alignment  */
+  MOE_ERR_CUDA = 2,          /* a CUDA launch or copy failed                           */
+  MOE_ERR_BAD_EXPERT_ID = 3, /* device: some topk_idx entry was >= E                   */
+  MOE_ERR_CAPACITY = 4,      /* device: the layout needs more rows than capacity_rows  */
+  MOE_ERR_TIMEOUT = 5,       /* device: a bounded wait inside a kernel ran out         */
+  MOE_ERR_UNSUPPORTED = 6    /* host: sizes beyond what this build supports            */
+};
+
+/* Limits of this build. */
+#define MOE_MAX_TOPK 32
+#define MOE_MAX_EXPERTS 1024
+
+/* Problem description.  Plain values, copied by every call. */
+typedef struct moe_layout_desc {
+  int64_t num_tokens;  /* N >= 0                                  */
+  int32_t topk;        /* K, 1 <= K <= MOE_MAX_TOPK ([CS] §4.2)  */
+  int32_t num_experts; /* E, 1 <= E <= MOE_MAX_EXPERTS           */
+  int32_t num_ranks;   /* R >= 1, R divides E                     */
+  int32_t alignment;   /* A >= 1 ([CS] §7.1-§7.2)                */
+} moe_layout_desc;
+
+/*
+ * Bytes of device workspace the other calls need for this description
+ * (sticky error word, per-tile expert and rank histograms).  The workspace
+ * must be zero-filled once before its first use (e.g. cudaMemsetAsync);
+ * afterwards the calls keep it consistent.  One workspace serves one stream
+ * at a time.
+ */
+MOE_API int moe_layout_workspace_bytes(const moe_layout_desc* desc, size_t* bytes);
+
+/*
+ * Count ([CS] §4.2).  Reads topk_idx [N*K]; writes
+ *   expert_count[E]: number of (t, k) with topk_idx[t*K+k] == e;
+ *   rank_count[R]:   number of tokens with at least one valid id in rank r,
+ *                    each token counted once per rank (deduplicated);
+ * and the per-tile histograms in `workspace` that moe_layout_scan needs.
+ * Bad ids set MOE_ERR_BAD_EXPERT_ID in the workspace error word.
+ */
+MOE_API int moe_layout_count(const moe_layout_desc* desc, const int64_t* topk_idx,
+                     int32_t* expert_count, int32_t* rank_count,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Prefix sums and slot maps ([CS] §5.2-§5.5, §7.2, §6.4).  Must follow
+ * moe_layout_count on the same topk_idx, counts and workspace.  Writes
+ *   expert_offset[E+1]: exclusive sum of align(expert_count[e], A); expert
+ *                       e's segment is rows [expert_offset[e], expert_offset[e+1]);
+ *                       rank r's block starts at expert_offset[r*L];
+ *   rank_psum[R]:       inclusive sum of rank_count;
+ *   dst_slot[N*K]:      row of (t, k) in the receive buffer, -1 if masked;
+ *   src_idx[rows]:      token of each row, -1 for the alignment-gap rows;
+ *   total_rows[1]:      expert_offset[E] (device scalar).
+ * capacity_rows is the length of src_idx (and of the receive buffers).  If
+ * the layout needs more rows, MOE_ERR_CAPACITY is recorded, src_idx is not
+ * written and every dst_slot entry is -1.  A bound that never fails is
+ * N*K + E*(A-1).
+ */
+MOE_API int moe_layout_scan(const moe_layout_desc* desc, const int64_t* topk_idx,
+                    const int32_t* expert_count, const int32_t* rank_count,
+                    void* workspace, size_t workspace_bytes,
+                    int32_t* expert_offset, int32_t* rank_psum,
+                    int32_t* dst_slot, int32_t* src_idx, int64_t capacity_rows,
+                    int32_t* total_rows, void* stream);
+
+/*
+ * Expand-mode dispatch permute ([CS] §6.3-§6.4, §8.2) with zero padding
+ * ([CS] §7.3).  For every valid (t, k): recv_x row dst_slot[t*K+k] = x row t,
+ * copied byte for byte (any row dtype: bf16, fp8, ...).  If sf is non-NULL
+ * the scale-factor row sf[t] moves the same way into recv_sf.  With
+ * zero_pad != 0, rows [expert_offset[e] + expert_count[e], expert_offset[e+1])
+ * of recv_x (and recv_sf) are set to zero bytes.
+ *   x [N, row_bytes], recv_x [capacity_rows, row_bytes]: row_bytes a positive
+ *     multiple of 16, both base pointers 16-byte aligned;
+ *   sf [N, sf_row_bytes], recv_sf [capacity_rows, sf_row_bytes]: sf_row_bytes
+ *     a positive multiple of 4, pointers 4-byte aligned (NULL sf: no scale factors);
+ *   dst_slot, expert_offset, expert_count: as written by the calls above.
+ * Slots >= capacity_rows are not written and record MOE_ERR_CAPACITY.
+ */
+MOE_API int moe_dispatch_permute(const moe_layout_desc* desc, const void* x,
+                         int64_t row_bytes, const void* sf, int64_t sf_row_bytes,
+                         const int32_t* dst_slot, const int32_t* expert_offset,
+                         const int32_t* expert_count, void* recv_x, void* recv_sf,
+                         int64_t capacity_rows, int zero_pad, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/*
+ * Combine: the inverse of the dispatch.  The pages keep the slot map for it
+ * ([CS] §6.2) but print no arithmetic; this is the plain definition
+ *   out[t, h] = bf16( sum over k = 0..K-1 with dst_slot[t*K+k] >= 0 of
+ *                     weights[t*K+k] * float(expert_out[dst_slot[t*K+k], h]) )
+ * accumulated in fp32 from 0 in ascending k with one fused multiply-add per
+ * term, rounded once to bf16 (nearest, ties to even).  A token with no valid
+ * slot gets zeros.
+ *   expert_out bf16 [expert_out_rows, hidden]; out bf16 [N, hidden];
+ *   weights fp32 [N*K]; hidden a positive multiple of 8; expert_out and out
+ *   16-byte aligned.  Slots >= expert_out_rows are skipped and record
+ *   MOE_ERR_CAPACITY.
+ */
+MOE_API int moe_combine_unpermute(const moe_layout_desc* desc, const void* expert_out,
+                          int64_t expert_out_rows, int64_t hidden,
+                          const int32_t* dst_slot, const float* weights,
+                          void* out, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/*
+ * Synchronise `stream`, copy the workspace's sticky error word (the first
+ * device-side error since the last read; MOE_OK if none) into
+ * *device_error, and reset it to MOE_OK.
+ */
+MOE_API int moe_layout_get_error(void* workspace, int32_t* device_error, void* stream);
+
+/* Static, human-readable name of a status code. */
+MOE_API const char* moe_strerror(int status);
+
+/* Number of kernels this library has launched in this process so far. */
+MOE_API uint64_t moe_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_LAYOUT_H_ */
