@@ -119,9 +119,12 @@ def layout(topk_idx, num_experts: int, num_ranks: int, alignment: int,
 
 def permute(x_bytes: np.ndarray, dst_slot, expert_offset, expert_count, rows: int,
             sf_bytes: np.ndarray | None = None, zero_pad: bool = True,
-            lib: ctypes.CDLL | None = None):
+            lib: ctypes.CDLL | None = None, out: np.ndarray | None = None,
+            out_sf: np.ndarray | None = None):
     """Expand-mode row scatter.  ``x_bytes`` is uint8 [N, row_bytes]
-    (any row dtype viewed as bytes); returns ``(status, recv_x, recv_sf)``."""
+    (any row dtype viewed as bytes); returns ``(status, recv_x, recv_sf)``.
+    Without ``out`` the receive buffer is new and filled with 0xA5 bytes, so
+    rows the oracle leaves alone stay visible."""
     lib = lib or load()
     x = _as(x_bytes, np.uint8)
     dst = _as(dst_slot, np.int32)
@@ -130,13 +133,16 @@ def permute(x_bytes: np.ndarray, dst_slot, expert_offset, expert_count, rows: in
     N, rb = x.shape
     K = dst.shape[1] if dst.ndim == 2 else (dst.size // max(N, 1) if N else 1)
     E = cnt.shape[0]
-    # Fill with a non-zero byte so that rows the oracle leaves alone are visible.
-    recv = np.full((rows, rb), 0xA5, np.uint8)
+    if out is None:
+        recv = np.full((rows, rb), 0xA5, np.uint8)
+    else:
+        recv = out
+        assert recv.dtype == np.uint8 and recv.shape[1] == rb and recv.shape[0] >= rows
     sf = srb = recv_sf = None
     if sf_bytes is not None:
         sf = _as(sf_bytes, np.uint8)
         srb = sf.shape[1]
-        recv_sf = np.full((rows, srb), 0xA5, np.uint8)
+        recv_sf = np.full((rows, srb), 0xA5, np.uint8) if out_sf is None else out_sf
     st = lib.oracle_permute(N, K, _ptr(dst), _ptr(x), rb, _ptr(sf), srb or 0, E, _ptr(off),
                             _ptr(cnt), _ptr(recv), _ptr(recv_sf), rows, 1 if zero_pad else 0)
     return int(st), recv, recv_sf
@@ -164,7 +170,8 @@ def expert_scale(recv_x_bf16: np.ndarray, expert_offset, scale,
     return eo
 
 
-def combine(expert_out_bf16: np.ndarray, dst_slot, weights, lib: ctypes.CDLL | None = None) -> np.ndarray:
+def combine(expert_out_bf16: np.ndarray, dst_slot, weights, lib: ctypes.CDLL | None = None,
+            out: np.ndarray | None = None) -> np.ndarray:
     """Weighted top-k combine; bf16 bits [rows, H] in, bf16 bits [N, H] out."""
     lib = lib or load()
     eo = _as(expert_out_bf16, np.uint16)
@@ -172,7 +179,9 @@ def combine(expert_out_bf16: np.ndarray, dst_slot, weights, lib: ctypes.CDLL | N
     w = _as(weights, np.float32)
     N, K = dst.shape
     H = eo.shape[1]
-    out = np.empty((N, H), np.uint16)
+    if out is None:
+        out = np.empty((N, H), np.uint16)
+    assert out.dtype == np.uint16 and out.shape == (N, H) and out.flags["C_CONTIGUOUS"]
     lib.oracle_combine(N, K, _ptr(dst), _ptr(w), _ptr(eo), H, _ptr(out))
     return out
 

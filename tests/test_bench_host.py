@@ -1,0 +1,88 @@
+"""bench.py host logic on the CPU: the oracle slice runner, the reference arm's
+JSON line, and the max-over-ranks timing across two gloo ranks."""
+import json
+import os
+import socket
+import sys
+
+import numpy as np
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+REPO = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, REPO)
+
+import bench  # noqa: E402
+import oracle  # noqa: E402
+from counting_sort_bucketization_gb300 import workloads as wl  # noqa: E402
+
+
+@pytest.mark.parametrize("S", [256, 64, 100])
+def test_slices_of_a_pass_equal_the_pass(S):
+    w = wl.WORKLOADS["tiny"]
+    inp = wl.make(w)
+    r = bench.OracleRunner(w, inp)
+    r.recv[:] = 0xEE
+    r.out[:] = 0xEEEE
+    nslices = -(-w.num_tokens // S)
+    done = sum(r.step(i, S) for i in range(nslices))
+    assert done == w.num_tokens
+    full = oracle.layout(inp["topk_idx"].numpy(), w.num_experts, w.num_ranks, w.alignment)
+    rows = full["total_rows"]
+    x = inp["x"].view(torch.uint8).numpy().reshape(w.num_tokens, -1)
+    _, recv, _ = oracle.permute(x, full["dst_slot"], full["expert_offset"], full["expert_count"], rows)
+    np.testing.assert_array_equal(r.recv[:rows], recv)
+    eo = oracle.expert_scale(recv.view(np.uint16), full["expert_offset"], inp["expert_scale"].numpy())
+    np.testing.assert_array_equal(r.out, oracle.combine(eo, full["dst_slot"], inp["weights"].numpy()))
+
+
+def test_reference_arm_prints_one_line(capsys):
+    bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "4", "--warmup", "1",
+                "--ref-seconds", "2"])
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "tokens/s"
+    assert d["value"] > 0 and d["steps"] == 4 and d["warmup"] == 1 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"] == "tiny"
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, results):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    bench.init_dist(world, "gloo")
+    got = bench.reduce_max(float(rank + 1) * 1.5, world, torch.device("cpu"))
+    bench.barrier(world)
+    results[rank] = got
+    torch.distributed.destroy_process_group()
+
+
+def test_max_over_ranks_with_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as m:
+        results = m.dict()
+        port = _free_port()
+        procs = [ctx.Process(target=_rank_main, args=(r, 2, port, results)) for r in range(2)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(120)
+            assert p.exitcode == 0
+        assert dict(results) == {0: 3.0, 1: 3.0}
+
+
+
+def test_reference_arm_other_ranks_exit_without_work(capsys, monkeypatch):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "0"])
+    assert capsys.readouterr().out.strip() == ""
