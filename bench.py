@@ -96,7 +96,8 @@ def config_of(w: wl.Workload) -> dict:
     return {"workload": w.name, "num_tokens": w.num_tokens, "topk": w.topk, "num_experts": w.num_experts,
             "num_ranks": w.num_ranks, "alignment": w.alignment, "hidden": w.hidden, "row_dtype": w.row_dtype,
             "routing": w.routing, "mask_prob": w.mask_prob,
-            "l2": "flushed between steps (256 MiB write, outside the step's events)"}
+            "l2": "flushed before every step, outside the step's events: 256 MiB written, then a second "
+                  "256 MiB buffer read, so each step starts with a cold L2 holding no dirty lines"}
 
 
 class ClockSampler:
@@ -266,23 +267,26 @@ def run_native(args, rank, world, local):
         row_e = torch.searchsorted(off[1:], torch.arange(rows, device=dev), right=True)
         eo[:rows] = (recv[:rows].float() * inp["expert_scale"].to(dev)[row_e][:, None]).to(torch.bfloat16)
     assert lay.error() == 0, "device error during set-up"
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def flush_l2():
+        flush_w.zero_()
+        flush_r.max()
 
     def step(ev):
         ev[0].record(stream)
-        lay.count(idx_d)
+        lay.build(idx_d)
         ev[1].record(stream)
-        lay.scan(idx_d)
-        ev[2].record(stream)
         lay.permute(x_d, recv, sf_d, recv_sf)
-        ev[3].record(stream)
+        ev[2].record(stream)
         if do_combine:
             lay.combine(eo, wt_d, out)
-        ev[4].record(stream)
+        ev[3].record(stream)
 
-    new_events = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    new_events = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         step(new_events())
     torch.cuda.synchronize(dev)
     assert lay.error() == 0, "device error during warm-up"
@@ -296,7 +300,7 @@ def run_native(args, rank, world, local):
         sampler.__enter__()
     t_wall0 = time.perf_counter()
     for i in range(args.steps):
-        flush.zero_()
+        flush_l2()
         step(evs[i])
     torch.cuda.synchronize(dev)
     t_wall = time.perf_counter() - t_wall0
@@ -307,13 +311,13 @@ def run_native(args, rank, world, local):
     err = lay.error()
     assert err == 0, f"device error {err} in the timed region"
 
-    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in evs])   # ms
+    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in evs])   # ms
     step_ms = per.sum(axis=1)
     ms_per_step = reduce_max(float(step_ms.mean()), world, dev)
-    kern_ms = per.mean(axis=0)
+    kern_ms = per.mean(axis=0)     # layout (count + scan + rank), permute, combine
     ab = algorithmic_bytes(w, lay)
     value = world * N / (ms_per_step / 1e3)
-    dispatch_ms = float(kern_ms[:3].sum())
+    dispatch_ms = float(kern_ms[:2].sum())
 
     # End to end through the public API with host buffers: pinned inputs in,
     # the combined tokens (and the row total) back, copies inside the timing.
@@ -330,7 +334,7 @@ def run_native(args, rank, world, local):
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
     e2e_ms = []
     for i in range(e2e_steps + 2):
-        flush.zero_()
+        flush_l2()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         idx_d.copy_(idx_h, non_blocking=True)
@@ -338,8 +342,7 @@ def run_native(args, rank, world, local):
         wt_d.copy_(wt_h, non_blocking=True)
         if sf_h is not None:
             sf_d.copy_(sf_h, non_blocking=True)
-        lay.count(idx_d)
-        lay.scan(idx_d)
+        lay.build(idx_d)
         lay.permute(x_d, recv, sf_d, recv_sf)
         if do_combine:
             lay.combine(eo, wt_d, out)
@@ -357,7 +360,7 @@ def run_native(args, rank, world, local):
     if rank != 0:
         return
     peaks = measured_peaks()
-    permute_s = kern_ms[2] / 1e3
+    permute_s = kern_ms[1] / 1e3
     achieved = ab["permute"] / permute_s / 1e9
     traffic = None
     if PERMUTE_TRAFFIC and PERMUTE_TRAFFIC.get("sha256") == sources_sha256(PERMUTE_SOURCES) \
@@ -370,9 +373,9 @@ def run_native(args, rank, world, local):
         "roofline": {"kernel": "permute_kernel", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "peak_source": peaks["source"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "traffic": traffic, "algorithmic_bytes_per_launch": ab["permute"]},
-        "kernels_ms": {"count": kern_ms[0], "scan": kern_ms[1], "permute": kern_ms[2], "combine": kern_ms[3]},
+        "kernels_ms": {"layout": kern_ms[0], "permute": kern_ms[1], "combine": kern_ms[2]},
         "kernels_gbs": {"permute": ab["permute"] / permute_s / 1e9,
-                        "combine": (ab["combine"] / (kern_ms[3] / 1e3) / 1e9) if do_combine else None},
+                        "combine": (ab["combine"] / (kern_ms[2] / 1e3) / 1e9) if do_combine else None},
         "dispatch_tokens_per_s": world * N / (dispatch_ms / 1e3),
         "layout": {"valid_pairs": ab["P"], "rows": ab["rows"], "tokens_routed": ab["tokens_routed"]},
         "e2e": {"value": world * N / (e2e_step_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,

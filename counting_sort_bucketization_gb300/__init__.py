@@ -14,7 +14,8 @@ from __future__ import annotations
 import importlib
 
 _BINDING_NAMES = (
-    "Layout", "LayoutError", "workspace_bytes", "new_workspace", "layout_count", "layout_scan",
+    "Layout", "LayoutDesc", "LayoutError", "workspace_bytes", "new_workspace", "layout_count", "layout_scan",
+    "layout_build",
     "dispatch_permute", "combine_unpermute", "get_error", "kernel_launches", "strerror",
     "library_path", "load_library", "dispatch", "ERROR_NAMES",
 )

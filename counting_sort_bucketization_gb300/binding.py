@@ -53,7 +53,8 @@ _lib: ctypes.CDLL | None = None
 
 
 def library_path() -> str:
-    return _build.LIB_PATH
+    """The in-tree build, unless MOE_LAYOUT_LIBRARY names another build of the same library."""
+    return os.environ.get("MOE_LAYOUT_LIBRARY") or _build.LIB_PATH
 
 
 def load_library() -> ctypes.CDLL:
@@ -71,6 +72,7 @@ def load_library() -> ctypes.CDLL:
         lib.moe_layout_workspace_bytes.argtypes = [dp, ctypes.POINTER(ctypes.c_size_t)]
         lib.moe_layout_count.argtypes = [dp, p, p, p, p, sz, p]
         lib.moe_layout_scan.argtypes = [dp, p, p, p, p, sz, p, p, p, p, i64, p, p]
+        lib.moe_layout_build.argtypes = [dp, p, p, p, p, sz, p, p, p, p, i64, p, p]
         lib.moe_dispatch_permute.argtypes = [dp, p, i64, p, i64, p, p, p, p, p, i64, ctypes.c_int, p, sz, p]
         lib.moe_combine_unpermute.argtypes = [dp, p, i64, i64, p, p, p, p, sz, p]
         lib.moe_layout_get_error.argtypes = [p, ctypes.POINTER(i32), p]
@@ -78,7 +80,7 @@ def load_library() -> ctypes.CDLL:
         lib.moe_strerror.restype = ctypes.c_char_p
         lib.moe_kernel_launches.argtypes = []
         lib.moe_kernel_launches.restype = ctypes.c_uint64
-        for name in ("moe_layout_workspace_bytes", "moe_layout_count", "moe_layout_scan",
+        for name in ("moe_layout_workspace_bytes", "moe_layout_count", "moe_layout_scan", "moe_layout_build",
                      "moe_dispatch_permute", "moe_combine_unpermute", "moe_layout_get_error"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -158,6 +160,20 @@ def layout_scan(desc, topk_idx, expert_count, rank_count, workspace, expert_offs
     _check(st, "moe_layout_scan")
 
 
+def layout_build(desc, topk_idx, expert_count, rank_count, workspace, expert_offset, rank_psum, dst_slot,
+                 src_idx, total_rows, stream=None) -> None:
+    """layout_count + layout_scan in one call (one cooperative kernel when it fits)."""
+    N, K, E, R = int(desc.num_tokens), int(desc.topk), int(desc.num_experts), int(desc.num_ranks)
+    st = load_library().moe_layout_build(
+        ctypes.byref(_desc(desc)), _dev(topk_idx, "topk_idx", torch.int64, N * K),
+        _dev(expert_count, "expert_count", torch.int32, E), _dev(rank_count, "rank_count", torch.int32, R),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+        _dev(expert_offset, "expert_offset", torch.int32, E + 1), _dev(rank_psum, "rank_psum", torch.int32, R),
+        _dev(dst_slot, "dst_slot", torch.int32, N * K), _dev(src_idx, "src_idx", torch.int32),
+        src_idx.numel(), _dev(total_rows, "total_rows", torch.int32, 1), _stream(stream))
+    _check(st, "moe_layout_build")
+
+
 def _row_bytes(t: torch.Tensor, rows: int) -> int:
     if rows == 0:
         return t.shape[-1] * t.element_size() if t.dim() >= 2 else 0
@@ -233,9 +249,14 @@ class Layout:
         layout_scan(self.desc, topk_idx, self.expert_count, self.rank_count, self.workspace, self.expert_offset,
                     self.rank_psum, self.dst_slot, self.src_idx, self.total_rows, stream)
 
-    def build(self, topk_idx, stream=None):
-        self.count(topk_idx, stream)
-        self.scan(topk_idx, stream)
+    def build(self, topk_idx, stream=None, fused=True):
+        """The whole layout; ``fused=False`` runs the two-call path (count, then scan)."""
+        if fused:
+            layout_build(self.desc, topk_idx, self.expert_count, self.rank_count, self.workspace,
+                         self.expert_offset, self.rank_psum, self.dst_slot, self.src_idx, self.total_rows, stream)
+        else:
+            self.count(topk_idx, stream)
+            self.scan(topk_idx, stream)
         return self
 
     def permute(self, x, recv_x, sf=None, recv_sf=None, zero_pad=True, stream=None):

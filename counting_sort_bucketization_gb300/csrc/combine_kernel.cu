@@ -26,9 +26,14 @@
 namespace moe {
 namespace {
 
+#ifndef MOE_COMBINE_CTAS_PER_SM
+#define MOE_COMBINE_CTAS_PER_SM 8
+#endif
+
 constexpr int kCombineThreads = 256;
 constexpr int kKGroup = 8;              // expert rows loaded before their FMAs
 constexpr int kMaxTokensPerCta = 64;
+constexpr int kCtasPerSm = MOE_COMBINE_CTAS_PER_SM;   // grid sizing target
 
 __device__ __forceinline__ void fma_bf16x8(float (&acc)[8], float w, const uint4& v) {
   const uint32_t u[4] = {v.x, v.y, v.z, v.w};
@@ -53,6 +58,8 @@ __global__ void __launch_bounds__(kCombineThreads)
 
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * tokens_per_cta;
   const int ntok = static_cast<int>(max64(0, min64(tokens_per_cta, a.num_tokens - t0)));
+  ptx::grid_dependency_wait();
+  ptx::grid_dependency_launch_dependents();
   for (int i = threadIdx.x; i < ntok * K; i += kCombineThreads) {
     int s = __ldg(a.dst_slot + t0 * K + i);
     if (s >= a.expert_out_rows) {
@@ -103,14 +110,16 @@ __global__ void __launch_bounds__(kCombineThreads)
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
   const int sms = device_sm_count();
-  const int64_t target_ctas = 4ll * sms;
+  const int64_t target_ctas = static_cast<int64_t>(kCtasPerSm) * sms;
   int64_t tpc = ceil_div64(max64(a.num_tokens, 1), target_ctas);
   tpc = max64(1, min64(tpc, kMaxTokensPerCta));
   const int64_t grid = max64(1, ceil_div64(a.num_tokens, tpc));
   const size_t smem = (sizeof(int32_t) + sizeof(float)) * static_cast<size_t>(tpc) * a.topk;
-  combine_kernel<<<static_cast<unsigned>(grid), kCombineThreads, smem, stream>>>(a, static_cast<int>(tpc));
+  const cudaError_t st = launch_pdl(combine_kernel, dim3(static_cast<unsigned>(grid)), dim3(kCombineThreads), smem,
+                                    stream, a, static_cast<int>(tpc));
+  if (st != cudaSuccess) return st;
   count_launch();
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace moe

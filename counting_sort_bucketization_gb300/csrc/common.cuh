@@ -7,6 +7,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include "../../include/moe_layout.h"
 
@@ -50,11 +51,12 @@ inline TilePlan make_tile_plan(int64_t N, int K) {
   return p;
 }
 
-// Workspace: [error word | pad to 256 B][hist int32 E x T][rank hist int32 R x T]
-// hist[e][tile] is expert e's count in the tile; the column scan turns it
-// into the count of expert e in all earlier tiles.
+// Workspace: [error word, grid-barrier words | pad to 256 B][hist int32 E x T]
+// [rank hist int32 R x T].  hist[e][tile] is expert e's count in the tile;
+// the column scan turns it into the count of expert e in all earlier tiles.
 struct WorkspaceLayout {
   size_t err_off = 0;
+  size_t bar_off = 16;   // two unsigned: arrival counter, generation
   size_t hist_off = 256;
   size_t rhist_off = 0;
   size_t bytes = 0;
@@ -66,6 +68,27 @@ inline WorkspaceLayout make_workspace_layout(const moe_layout_desc& d, const Til
   w.rhist_off = w.hist_off + ((static_cast<size_t>(d.num_experts) * T * 4 + 255) / 256) * 256;
   w.bytes = w.rhist_off + ((static_cast<size_t>(d.num_ranks) * T * 4 + 255) / 256) * 256;
   return w;
+}
+
+// Launch with programmatic dependent launch allowed: the kernel may start
+// while the previous kernel on the stream is still running; it must execute
+// griddepcontrol.wait (ptx::grid_dependency_wait) before it reads anything
+// an earlier kernel wrote.  With any other predecessor (a copy, a kernel that
+// never triggers) it behaves like an ordinary launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // First error wins; later ones are dropped.

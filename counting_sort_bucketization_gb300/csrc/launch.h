@@ -24,6 +24,14 @@ cudaError_t launch_rank(const moe_layout_desc& d, const TilePlan& p, const int64
                         int32_t* dst_slot, int32_t* src_idx, int64_t capacity,
                         int32_t* total_rows, int* err, cudaStream_t stream);
 
+// Count + scan + rank: one cooperative kernel when every tile fits on the
+// GPU at once, else the three kernels above.
+cudaError_t launch_build(const moe_layout_desc& d, const TilePlan& p, const int64_t* topk_idx,
+                         int32_t* expert_count, int32_t* rank_count, int32_t* hist, int32_t* rhist,
+                         unsigned* barrier_words, int32_t* expert_offset, int32_t* rank_psum, int32_t* dst_slot,
+                         int32_t* src_idx, int64_t capacity, int32_t* total_rows, int* err,
+                         cudaStream_t stream);
+
 struct PermuteArgs {
   const uint8_t* x;
   const uint8_t* sf;

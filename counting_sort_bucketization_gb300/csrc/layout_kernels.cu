@@ -11,14 +11,21 @@
 //   scan    [CS] §5.2-§5.5, §7.2: the page scans on one SM after a grid-wide
 //           reduction; here one warp per expert scans that expert's tile
 //           column, and every rank CTA recomputes the (small) aligned
-//           exclusive sum over experts itself, so no kernel waits on another
-//           SM inside a launch.
+//           exclusive sum over experts itself.
 //   rank    [CS] §6.4 assigns slots with atomicAdd on the exclusive sum,
 //           which makes the order inside a segment depend on scheduling.
 //           Here the slot is expert_offset[e] + (pairs of e in earlier
 //           tiles) + (pairs of e earlier in this tile), the last term from
 //           __match_any_sync + popc within a warp and a per-expert scan over
 //           the warps: token-ascending and deterministic.
+//
+// Two ways to run the three phases:
+//   - three kernels (count_tiles, scan_columns, rank_maps), chained with
+//     programmatic dependent launch;
+//   - one cooperative kernel (layout_fused_kernel) with two grid barriers,
+//     used when every tile's CTA fits on the GPU at once.  The tile's ids stay
+//     in shared memory from the count to the rank phase, and two launches and
+//     their gaps disappear.  Its barrier waits are bounded (MOE_ERR_TIMEOUT).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -59,25 +66,25 @@ __device__ __forceinline__ int warp_inclusive_scan(int v, int lane) {
   return v;
 }
 
-// ----------------------------------------------------------------- count
-__global__ void __launch_bounds__(kLayoutThreads)
-    count_tiles_kernel(const int64_t* __restrict__ topk_idx, int64_t N, int K, int E, int R,
-                       TilePlan plan, int32_t* __restrict__ hist, int32_t* __restrict__ rhist,
-                       int* err) {
-  extern __shared__ int smem[];
-  int* hist_s = smem;         // [E]
-  int* rhist_s = smem + E;    // [R]
-  int* ids_s = rhist_s + R;   // [tile pairs]
-  const int tile = blockIdx.x;
-  const int64_t T = plan.tiles;
-  const int64_t t0 = static_cast<int64_t>(tile) * plan.tile_tokens;
-  const int ntok = static_cast<int>(min64(plan.tile_tokens, N - t0));
+struct TileCoords {
+  int64_t t0;   // first token of the tile
+  int ntok;     // tokens in the tile (the last tile may be short)
+};
+
+__device__ __forceinline__ TileCoords tile_coords(const TilePlan& plan, int64_t N, int tile) {
+  TileCoords c;
+  c.t0 = static_cast<int64_t>(tile) * plan.tile_tokens;
+  c.ntok = static_cast<int>(max64(0, min64(plan.tile_tokens, N - c.t0)));
+  return c;
+}
+
+// ------------------------------------------------------- phase: count
+// ids_s holds the tile's staged ids; hist_s [E] and rhist_s [R] are zeroed.
+// Writes the tile's column of hist [E][T] and rhist [R][T].
+__device__ void count_phase(const TilePlan& plan, int K, int E, int R, int tile, int ntok,
+                            const int* ids_s, int* hist_s, int* rhist_s, int32_t* __restrict__ hist,
+                            int32_t* __restrict__ rhist) {
   const int L = E / R;
-
-  for (int i = threadIdx.x; i < E + R; i += blockDim.x) smem[i] = 0;
-  stage_tile_ids(topk_idx, t0 * K, ntok * K, E, ids_s, err);
-  __syncthreads();
-
   const int warp = threadIdx.x / kWarpSize, lane = threadIdx.x % kWarpSize;
   const int tok_in_chunk = lane / K;
   for (int c = 0; c < plan.cpw; ++c) {
@@ -99,68 +106,68 @@ __global__ void __launch_bounds__(kLayoutThreads)
     if (valid && __ffs(rpeers) - 1 == lane) atomicAdd(&rhist_s[r], 1);
   }
   __syncthreads();
+  const int64_t T = plan.tiles;
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[static_cast<int64_t>(e) * T + tile] = hist_s[e];
   for (int r = threadIdx.x; r < R; r += blockDim.x) rhist[static_cast<int64_t>(r) * T + tile] = rhist_s[r];
 }
 
-// ----------------------------------------------------------- column scan
-// One warp per row: expert rows become exclusive prefixes over tiles and
-// give expert_count; rank rows give rank_count.
-__global__ void __launch_bounds__(kLayoutThreads)
-    scan_columns_kernel(int32_t* __restrict__ hist, const int32_t* __restrict__ rhist, int64_t T,
-                        int E, int R, int32_t* __restrict__ expert_count,
-                        int32_t* __restrict__ rank_count) {
+// ------------------------------------------------- phase: column scan
+// Warp w of CTA b scans rows b*kLayoutWarps + w, + gridDim.x*kLayoutWarps, ...
+// Expert rows become exclusive prefixes over tiles and give expert_count;
+// rank rows give rank_count.  Loads go through L2 (__ldcg): in the fused
+// kernel other CTAs wrote these rows earlier in the same launch.
+__device__ void scan_phase(int32_t* __restrict__ hist, const int32_t* __restrict__ rhist, int64_t T, int E,
+                           int R, int32_t* __restrict__ expert_count, int32_t* __restrict__ rank_count) {
   const int warp = threadIdx.x / kWarpSize, lane = threadIdx.x % kWarpSize;
-  const int row = blockIdx.x * kLayoutWarps + warp;
-  if (row >= E + R) return;
-  const bool is_expert = row < E;
-  const int32_t* src = is_expert ? hist + static_cast<int64_t>(row) * T
-                                 : rhist + static_cast<int64_t>(row - E) * T;
   const int64_t m = ceil_div64(T, kWarpSize);
   const int64_t lo = min64(lane * m, T), hi = min64(lo + m, T);
-  int sum = 0;
-  for (int64_t i = lo; i < hi; ++i) sum += src[i];
-  const int incl = warp_inclusive_scan(sum, lane);
-  const int total = __shfl_sync(kFull, incl, kWarpSize - 1);
-  if (is_expert) {
-    int32_t* dst = hist + static_cast<int64_t>(row) * T;
-    int run = incl - sum;
-    for (int64_t i = lo; i < hi; ++i) {
-      const int c = dst[i];
-      dst[i] = run;
-      run += c;
+  for (int row = blockIdx.x * kLayoutWarps + warp; row < E + R; row += gridDim.x * kLayoutWarps) {
+    const bool is_expert = row < E;
+    const int32_t* src = is_expert ? hist + static_cast<int64_t>(row) * T
+                                   : rhist + static_cast<int64_t>(row - E) * T;
+    int sum = 0;
+    for (int64_t i = lo; i < hi; ++i) sum += __ldcg(src + i);
+    const int incl = warp_inclusive_scan(sum, lane);
+    const int total = __shfl_sync(kFull, incl, kWarpSize - 1);
+    if (is_expert) {
+      int32_t* dst = hist + static_cast<int64_t>(row) * T;
+      int run = incl - sum;
+      for (int64_t i = lo; i < hi; ++i) {
+        const int c = __ldcg(dst + i);
+        dst[i] = run;
+        run += c;
+      }
+      if (lane == 0) expert_count[row] = total;
+    } else if (lane == 0) {
+      rank_count[row - E] = total;
     }
-    if (lane == 0) expert_count[row] = total;
-  } else if (lane == 0) {
-    rank_count[row - E] = total;
   }
 }
 
-// ------------------------------------------------------------ rank + maps
-__global__ void __launch_bounds__(kLayoutThreads)
-    rank_maps_kernel(const int64_t* __restrict__ topk_idx, int64_t N, int K, int E, int R, int A,
-                     TilePlan plan, const int32_t* __restrict__ hist_prefix,
-                     const int32_t* __restrict__ expert_count,
-                     const int32_t* __restrict__ rank_count, int32_t* __restrict__ expert_offset,
-                     int32_t* __restrict__ rank_psum, int32_t* __restrict__ dst_slot,
-                     int32_t* __restrict__ src_idx, int64_t capacity, int32_t* __restrict__ total_rows,
-                     int* err) {
-  extern __shared__ int smem[];
-  int* off_s = smem;                          // [E+1] aligned exclusive offsets
-  int* cnt_s = off_s + (E + 1);               // [kLayoutWarps][E] per-warp counters, then bases
-  int* ids_s = cnt_s + kLayoutWarps * E;      // [tile pairs]
-  int* lr_s = ids_s + plan.tile_tokens * K;   // [tile pairs] rank inside the warp's run
-  __shared__ int warp_tot_s[kLayoutWarps];
+// -------------------------------------------------- phase: rank + maps
+struct RankArgs {
+  int64_t N;
+  int K, E, R, A;
+  const int32_t* hist_prefix;   // [E][T] exclusive prefixes over tiles
+  const int32_t* expert_count;
+  const int32_t* rank_count;
+  int32_t* expert_offset;
+  int32_t* rank_psum;
+  int32_t* dst_slot;
+  int32_t* src_idx;
+  int64_t capacity;
+  int32_t* total_rows;
+  int* err;
+};
 
-  const int tile = blockIdx.x;
+// ids_s holds the tile's staged ids; off_s [E+1], cnt_s [kLayoutWarps*E]
+// (zeroed), lr_s [tile pairs] are shared scratch.
+__device__ void rank_phase(const TilePlan& plan, const RankArgs& a, int tile, TileCoords tc, const int* ids_s,
+                           int* off_s, int* cnt_s, int* lr_s, int* warp_tot_s) {
+  const int K = a.K, E = a.E, R = a.R, A = a.A;
   const int64_t T = plan.tiles;
-  const int64_t t0 = static_cast<int64_t>(tile) * plan.tile_tokens;
-  const int ntok = static_cast<int>(max64(0, min64(plan.tile_tokens, N - t0)));
-  const int npairs = ntok * K;
+  const int npairs = tc.ntok * K;
   const int warp = threadIdx.x / kWarpSize, lane = threadIdx.x % kWarpSize;
-
-  for (int i = threadIdx.x; i < kLayoutWarps * E; i += blockDim.x) cnt_s[i] = 0;
-  stage_tile_ids(topk_idx, t0 * K, npairs, E, ids_s, err);
 
   // Aligned exclusive sum over experts ([CS] §7.2 then §5.5), block-wide.
   // Thread i owns experts [i*ipt, (i+1)*ipt).
@@ -169,7 +176,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
   int mine = 0;
   for (int j = 0; j < ipt; ++j) {
     const int e = e_lo + j;
-    if (e < E) mine += static_cast<int>(ceil_div64(__ldg(expert_count + e), A) * A);
+    if (e < E) mine += static_cast<int>(ceil_div64(__ldcg(a.expert_count + e), A) * A);
   }
   const int incl = warp_inclusive_scan(mine, lane);
   if (lane == kWarpSize - 1) warp_tot_s[warp] = incl;
@@ -181,27 +188,27 @@ __global__ void __launch_bounds__(kLayoutThreads)
     const int e = e_lo + j;
     if (e < E) {
       off_s[e] = run;
-      run += static_cast<int>(ceil_div64(__ldg(expert_count + e), A) * A);
+      run += static_cast<int>(ceil_div64(__ldcg(a.expert_count + e), A) * A);
     }
   }
   if (threadIdx.x == kLayoutThreads - 1) off_s[E] = run;
   __syncthreads();
   const int64_t rows = off_s[E];
-  const bool cap_ok = rows <= capacity;
+  const bool cap_ok = rows <= a.capacity;
 
   if (tile == 0) {
-    for (int e = threadIdx.x; e <= E; e += blockDim.x) expert_offset[e] = off_s[e];
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) a.expert_offset[e] = off_s[e];
     if (threadIdx.x == 0) {
-      *total_rows = static_cast<int32_t>(rows);
-      if (!cap_ok) set_error(err, MOE_ERR_CAPACITY);
+      *a.total_rows = static_cast<int32_t>(rows);
+      if (!cap_ok) set_error(a.err, MOE_ERR_CAPACITY);
     }
     if (warp == 0) {  // inclusive sum over ranks ([CS] §5.5)
       int carry = 0;
       for (int base = 0; base < R; base += kWarpSize) {
         const int r = base + lane;
-        const int v = r < R ? __ldg(rank_count + r) : 0;
+        const int v = r < R ? __ldcg(a.rank_count + r) : 0;
         const int s = warp_inclusive_scan(v, lane) + carry;
-        if (r < R) rank_psum[r] = s;
+        if (r < R) a.rank_psum[r] = s;
         carry = __shfl_sync(kFull, s, kWarpSize - 1);
       }
     }
@@ -213,7 +220,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
   for (int c = 0; c < plan.cpw; ++c) {
     const int chunk = warp * plan.cpw + c;
     const int tok = chunk * plan.tpc + tok_in_chunk;
-    const bool in = lane < plan.lanes && tok < ntok;
+    const bool in = lane < plan.lanes && tok < tc.ntok;
     const int pair = chunk * plan.lanes + lane;
     const int e = in ? ids_s[pair] : -1;
     const bool valid = e >= 0;
@@ -231,7 +238,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
 
   // Per expert: turn the per-warp counts into absolute slot bases.
   for (int e = threadIdx.x; e < E && tile < T; e += blockDim.x) {
-    int b = off_s[e] + hist_prefix[static_cast<int64_t>(e) * T + tile];
+    int b = off_s[e] + __ldcg(a.hist_prefix + static_cast<int64_t>(e) * T + tile);
     for (int w = 0; w < kLayoutWarps; ++w) {
       const int c = cnt_s[w * E + e];
       cnt_s[w * E + e] = b;
@@ -247,18 +254,163 @@ __global__ void __launch_bounds__(kLayoutThreads)
     int slot = -1;
     if (e >= 0 && cap_ok) {
       slot = cnt_s[(i / pairs_per_warp) * E + e] + lr_s[i];
-      src_idx[slot] = static_cast<int32_t>(t0 + i / K);
+      a.src_idx[slot] = static_cast<int32_t>(tc.t0 + i / K);
     }
-    dst_slot[t0 * K + i] = slot;
+    a.dst_slot[tc.t0 * K + i] = slot;
   }
 
   // Alignment-gap rows have no source token.
   if (cap_ok) {
     for (int e = tile; e < E; e += gridDim.x) {
-      const int lo = off_s[e] + __ldg(expert_count + e), hi = off_s[e + 1];
-      for (int row = lo + threadIdx.x; row < hi; row += blockDim.x) src_idx[row] = -1;
+      const int lo = off_s[e] + __ldcg(a.expert_count + e), hi = off_s[e + 1];
+      for (int row = lo + threadIdx.x; row < hi; row += blockDim.x) a.src_idx[row] = -1;
     }
   }
+}
+
+// ---------------------------------------------------------- kernels
+__global__ void __launch_bounds__(kLayoutThreads)
+    count_tiles_kernel(const int64_t* __restrict__ topk_idx, int64_t N, int K, int E, int R,
+                       TilePlan plan, int32_t* __restrict__ hist, int32_t* __restrict__ rhist,
+                       int* err) {
+  extern __shared__ int smem[];
+  int* hist_s = smem;         // [E]
+  int* rhist_s = smem + E;    // [R]
+  int* ids_s = rhist_s + R;   // [tile pairs]
+  const TileCoords tc = tile_coords(plan, N, blockIdx.x);
+  for (int i = threadIdx.x; i < E + R; i += blockDim.x) smem[i] = 0;
+  ptx::grid_dependency_wait();
+  ptx::grid_dependency_launch_dependents();
+  stage_tile_ids(topk_idx, tc.t0 * K, tc.ntok * K, E, ids_s, err);
+  __syncthreads();
+  count_phase(plan, K, E, R, blockIdx.x, tc.ntok, ids_s, hist_s, rhist_s, hist, rhist);
+}
+
+__global__ void __launch_bounds__(kLayoutThreads)
+    scan_columns_kernel(int32_t* __restrict__ hist, const int32_t* __restrict__ rhist, int64_t T,
+                        int E, int R, int32_t* __restrict__ expert_count,
+                        int32_t* __restrict__ rank_count) {
+  ptx::grid_dependency_wait();
+  ptx::grid_dependency_launch_dependents();
+  scan_phase(hist, rhist, T, E, R, expert_count, rank_count);
+}
+
+__global__ void __launch_bounds__(kLayoutThreads)
+    rank_maps_kernel(const int64_t* __restrict__ topk_idx, TilePlan plan, RankArgs a) {
+  extern __shared__ int smem[];
+  int* off_s = smem;                            // [E+1]
+  int* cnt_s = off_s + (a.E + 1);               // [kLayoutWarps][E]
+  int* ids_s = cnt_s + kLayoutWarps * a.E;      // [tile pairs]
+  int* lr_s = ids_s + plan.tile_tokens * a.K;   // [tile pairs]
+  __shared__ int warp_tot_s[kLayoutWarps];
+  const TileCoords tc = tile_coords(plan, a.N, blockIdx.x);
+  for (int i = threadIdx.x; i < kLayoutWarps * a.E; i += blockDim.x) cnt_s[i] = 0;
+  ptx::grid_dependency_wait();
+  ptx::grid_dependency_launch_dependents();
+  stage_tile_ids(topk_idx, tc.t0 * a.K, tc.ntok * a.K, a.E, ids_s, a.err);
+  rank_phase(plan, a, blockIdx.x, tc, ids_s, off_s, cnt_s, lr_s, warp_tot_s);
+}
+
+// Grid-wide barrier for a cooperative launch: arrive on a counter; the last
+// CTA resets it and bumps the generation the others wait on.  The wait is
+// bounded; on timeout the error word gets MOE_ERR_TIMEOUT and the CTA stops.
+__device__ bool grid_barrier(unsigned* arrive, unsigned* gen, unsigned nctas, int* err, int* flag_s) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bool ok = true;
+    const unsigned g0 = ptx::ld_acquire_gpu(gen);
+    __threadfence();
+    if (atomicAdd(arrive, 1u) == nctas - 1) {
+      atomicExch(arrive, 0u);
+      __threadfence();
+      atomicAdd(gen, 1u);
+    } else {
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (ptx::ld_acquire_gpu(gen) == g0) {
+        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+          set_error(err, MOE_ERR_TIMEOUT);
+          ok = false;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    __threadfence();
+    *flag_s = ok ? 1 : 0;
+  }
+  __syncthreads();
+  return *flag_s != 0;
+}
+
+__global__ void __launch_bounds__(kLayoutThreads)
+    layout_fused_kernel(const int64_t* __restrict__ topk_idx, TilePlan plan, RankArgs a, int32_t* hist,
+                        int32_t* rhist, int32_t* expert_count, int32_t* rank_count, unsigned* bar) {
+  extern __shared__ int smem[];
+  const int E = a.E, R = a.R, K = a.K;
+  int* ids_s = smem;                            // [tile pairs], kept across all phases
+  int* lr_s = ids_s + plan.tile_tokens * K;     // [tile pairs]
+  int* cnt_s = lr_s + plan.tile_tokens * K;     // [kLayoutWarps][E]; its first E + R ints
+                                                // serve as the count phase's histograms
+  int* off_s = cnt_s + kLayoutWarps * E;        // [E+1]
+  __shared__ int warp_tot_s[kLayoutWarps];
+  __shared__ int flag_s;
+  const TileCoords tc = tile_coords(plan, a.N, blockIdx.x);
+  int* hist_s = cnt_s;
+  int* rhist_s = cnt_s + E;
+  for (int i = threadIdx.x; i < E + R; i += blockDim.x) hist_s[i] = 0;
+  ptx::grid_dependency_wait();
+  ptx::grid_dependency_launch_dependents();
+  stage_tile_ids(topk_idx, tc.t0 * K, tc.ntok * K, E, ids_s, a.err);
+  __syncthreads();
+  count_phase(plan, K, E, R, blockIdx.x, tc.ntok, ids_s, hist_s, rhist_s, hist, rhist);
+  if (!grid_barrier(bar, bar + 1, gridDim.x, a.err, &flag_s)) return;
+  scan_phase(hist, rhist, plan.tiles, E, R, expert_count, rank_count);
+  for (int i = threadIdx.x; i < kLayoutWarps * E; i += blockDim.x) cnt_s[i] = 0;
+  if (!grid_barrier(bar, bar + 1, gridDim.x, a.err, &flag_s)) return;
+  rank_phase(plan, a, blockIdx.x, tc, ids_s, off_s, cnt_s, lr_s, warp_tot_s);
+}
+
+size_t fused_smem_bytes(const moe_layout_desc& d, const TilePlan& p) {
+  const size_t pairs = static_cast<size_t>(p.tile_tokens) * d.topk;
+  const size_t E = d.num_experts;
+  return sizeof(int) * (2 * pairs + kLayoutWarps * E + E + 1);
+}
+
+// Whether every tile's CTA of the fused kernel can be resident at once.
+bool fused_fits(const TilePlan& p, size_t smem) {
+  int dev = 0, coop = 0, per_sm = 0;
+  if (p.tiles < 1) return false;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop) return false;
+  if (cudaFuncSetAttribute(layout_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return false;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layout_fused_kernel, kLayoutThreads, smem) !=
+      cudaSuccess)
+    return false;
+  return p.tiles <= static_cast<int64_t>(per_sm) * device_sm_count();
+}
+
+RankArgs rank_args(const moe_layout_desc& d, const int32_t* hist_prefix, const int32_t* expert_count,
+                   const int32_t* rank_count, int32_t* expert_offset, int32_t* rank_psum, int32_t* dst_slot,
+                   int32_t* src_idx, int64_t capacity, int32_t* total_rows, int* err) {
+  RankArgs a;
+  a.N = d.num_tokens;
+  a.K = d.topk;
+  a.E = d.num_experts;
+  a.R = d.num_ranks;
+  a.A = d.alignment;
+  a.hist_prefix = hist_prefix;
+  a.expert_count = expert_count;
+  a.rank_count = rank_count;
+  a.expert_offset = expert_offset;
+  a.rank_psum = rank_psum;
+  a.dst_slot = dst_slot;
+  a.src_idx = src_idx;
+  a.capacity = capacity;
+  a.total_rows = total_rows;
+  a.err = err;
+  return a;
 }
 
 }  // namespace
@@ -283,17 +435,17 @@ cudaError_t launch_count(const moe_layout_desc& d, const TilePlan& p, const int6
                                         static_cast<int>(smem1));
   if (st != cudaSuccess) return st;
   if (p.tiles > 0) {
-    count_tiles_kernel<<<static_cast<unsigned>(p.tiles), kLayoutThreads, smem1, stream>>>(
-        topk_idx, d.num_tokens, d.topk, d.num_experts, d.num_ranks, p, hist, rhist, err);
-    count_launch();
-    st = cudaGetLastError();
+    st = launch_pdl(count_tiles_kernel, dim3(static_cast<unsigned>(p.tiles)), dim3(kLayoutThreads), smem1,
+                    stream, topk_idx, d.num_tokens, d.topk, d.num_experts, d.num_ranks, p, hist, rhist, err);
     if (st != cudaSuccess) return st;
+    count_launch();
   }
   const int rows = d.num_experts + d.num_ranks;
-  scan_columns_kernel<<<(rows + kLayoutWarps - 1) / kLayoutWarps, kLayoutThreads, 0, stream>>>(
-      hist, rhist, p.tiles, d.num_experts, d.num_ranks, expert_count, rank_count);
+  st = launch_pdl(scan_columns_kernel, dim3((rows + kLayoutWarps - 1) / kLayoutWarps), dim3(kLayoutThreads), 0,
+                  stream, hist, rhist, p.tiles, d.num_experts, d.num_ranks, expert_count, rank_count);
+  if (st != cudaSuccess) return st;
   count_launch();
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 cudaError_t launch_rank(const moe_layout_desc& d, const TilePlan& p, const int64_t* topk_idx,
@@ -307,12 +459,44 @@ cudaError_t launch_rank(const moe_layout_desc& d, const TilePlan& p, const int64
                                         static_cast<int>(smem));
   if (st != cudaSuccess) return st;
   const int64_t grid = p.tiles > 0 ? p.tiles : 1;
-  rank_maps_kernel<<<static_cast<unsigned>(grid), kLayoutThreads, smem, stream>>>(
-      topk_idx, d.num_tokens, d.topk, d.num_experts, d.num_ranks, d.alignment, p, hist_prefix,
-      expert_count, rank_count, expert_offset, rank_psum, dst_slot, src_idx, capacity,
-      total_rows, err);
+  const RankArgs a = rank_args(d, hist_prefix, expert_count, rank_count, expert_offset, rank_psum, dst_slot,
+                               src_idx, capacity, total_rows, err);
+  st = launch_pdl(rank_maps_kernel, dim3(static_cast<unsigned>(grid)), dim3(kLayoutThreads), smem, stream,
+                  topk_idx, p, a);
+  if (st != cudaSuccess) return st;
   count_launch();
-  return cudaGetLastError();
+  return cudaSuccess;
+}
+
+cudaError_t launch_build(const moe_layout_desc& d, const TilePlan& p, const int64_t* topk_idx,
+                         int32_t* expert_count, int32_t* rank_count, int32_t* hist, int32_t* rhist,
+                         unsigned* barrier_words, int32_t* expert_offset, int32_t* rank_psum, int32_t* dst_slot,
+                         int32_t* src_idx, int64_t capacity, int32_t* total_rows, int* err,
+                         cudaStream_t stream) {
+  const size_t smem = fused_smem_bytes(d, p);
+  if (!fused_fits(p, smem)) {
+    cudaError_t st = launch_count(d, p, topk_idx, expert_count, rank_count, err, hist, rhist, stream);
+    if (st != cudaSuccess) return st;
+    return launch_rank(d, p, topk_idx, hist, expert_count, rank_count, expert_offset, rank_psum, dst_slot,
+                       src_idx, capacity, total_rows, err, stream);
+  }
+  const RankArgs a = rank_args(d, hist, expert_count, rank_count, expert_offset, rank_psum, dst_slot, src_idx,
+                               capacity, total_rows, err);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.tiles));
+  cfg.blockDim = dim3(kLayoutThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t st = cudaLaunchKernelEx(&cfg, layout_fused_kernel, topk_idx, p, a, hist, rhist,
+                                            expert_count, rank_count, barrier_words);
+  if (st != cudaSuccess) return st;
+  count_launch();
+  return cudaSuccess;
 }
 
 }  // namespace moe

@@ -108,6 +108,25 @@ int moe_layout_scan(const moe_layout_desc* desc, const int64_t* topk_idx, const 
                                  total_rows, at<int>(workspace, w.err_off), static_cast<cudaStream_t>(stream)));
 }
 
+int moe_layout_build(const moe_layout_desc* desc, const int64_t* topk_idx, int32_t* expert_count,
+                     int32_t* rank_count, void* workspace, size_t workspace_bytes, int32_t* expert_offset,
+                     int32_t* rank_psum, int32_t* dst_slot, int32_t* src_idx, int64_t capacity_rows,
+                     int32_t* total_rows, void* stream) {
+  if (int st = check_desc(desc)) return st;
+  WorkspaceLayout w;
+  if (int st = check_workspace(desc, workspace, workspace_bytes, &w)) return st;
+  const bool has_pairs = desc->num_tokens > 0;
+  if ((has_pairs && (topk_idx == nullptr || dst_slot == nullptr)) || expert_count == nullptr ||
+      rank_count == nullptr || expert_offset == nullptr || rank_psum == nullptr || total_rows == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (capacity_rows < 0 || (capacity_rows > 0 && src_idx == nullptr)) return MOE_ERR_INVALID_ARG;
+  const TilePlan p = make_tile_plan(desc->num_tokens, desc->topk);
+  return cuda_status(launch_build(*desc, p, topk_idx, expert_count, rank_count, at<int32_t>(workspace, w.hist_off),
+                                  at<int32_t>(workspace, w.rhist_off), at<unsigned>(workspace, w.bar_off),
+                                  expert_offset, rank_psum, dst_slot, src_idx, capacity_rows, total_rows,
+                                  at<int>(workspace, w.err_off), static_cast<cudaStream_t>(stream)));
+}
+
 int moe_dispatch_permute(const moe_layout_desc* desc, const void* x, int64_t row_bytes, const void* sf,
                          int64_t sf_row_bytes, const int32_t* dst_slot, const int32_t* expert_offset,
                          const int32_t* expert_count, void* recv_x, void* recv_sf, int64_t capacity_rows,

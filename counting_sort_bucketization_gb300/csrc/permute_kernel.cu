@@ -29,11 +29,19 @@
 namespace moe {
 namespace {
 
+#ifndef MOE_PERMUTE_CTAS_PER_SM
+#define MOE_PERMUTE_CTAS_PER_SM 4
+#endif
+#ifndef MOE_PERMUTE_STAGE_BUDGET
+#define MOE_PERMUTE_STAGE_BUDGET (48 * 1024)
+#endif
+
 constexpr int kPermuteThreads = 256;
 constexpr int kPermuteWarps = kPermuteThreads / kWarpSize;
 constexpr int kMaxStages = 8;
 constexpr int kMaxChunkBytes = 16384;
-constexpr int kStageBudgetBytes = 64 * 1024;
+constexpr int kStageBudgetBytes = MOE_PERMUTE_STAGE_BUDGET;  // shared-memory ring per CTA
+constexpr int kCtasPerSm = MOE_PERMUTE_CTAS_PER_SM;           // grid sizing target
 constexpr int kMaxTokensPerCta = 512;
 constexpr int kSfRegWords = 4;  // scale-factor words a lane keeps in registers
 
@@ -95,6 +103,12 @@ __global__ void __launch_bounds__(kPermuteThreads)
   const int warp = threadIdx.x / kWarpSize, lane = threadIdx.x % kWarpSize;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * p.tokens_per_cta;
   const int ntok = static_cast<int>(max64(0, min64(p.tokens_per_cta, a.num_tokens - t0)));
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) ptx::mbar_init(&full_bar[s], 1);
+    ptx::fence_mbar_init();
+  }
+  ptx::grid_dependency_wait();
+  ptx::grid_dependency_launch_dependents();
   const int64_t rows = __ldg(a.expert_offset + E);
   if (rows > a.capacity) {
     if (blockIdx.x == 0 && threadIdx.x == 0) set_error(a.err, MOE_ERR_CAPACITY);
@@ -110,10 +124,6 @@ __global__ void __launch_bounds__(kPermuteThreads)
     slots_s[i] = s;
   }
   if (a.zero_pad) gap_prefix(a.expert_offset, a.expert_count, E, padpre_s, warp_tot_s);
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < p.stages; ++s) ptx::mbar_init(&full_bar[s], 1);
-    ptx::fence_mbar_init();
-  }
   __syncthreads();
 
   if (warp == 0) {
@@ -250,7 +260,7 @@ PermutePlan make_permute_plan(const PermuteArgs& a, int sms) {
   p.chunk_bytes = static_cast<int>(min64(a.row_bytes, kMaxChunkBytes));
   p.nchunks = static_cast<int>(ceil_div64(a.row_bytes, p.chunk_bytes));
   p.stages = std::max(2, std::min(kMaxStages, kStageBudgetBytes / p.chunk_bytes));
-  const int64_t target_ctas = 2ll * sms;
+  const int64_t target_ctas = static_cast<int64_t>(kCtasPerSm) * sms;
   int64_t tpc = ceil_div64(max64(a.num_tokens, 1), target_ctas);
   tpc = max64(1, min64(tpc, kMaxTokensPerCta));
   p.tokens_per_cta = static_cast<int>(tpc);
@@ -273,9 +283,10 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t stream) {
   cudaError_t st = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(p.smem));
   if (st != cudaSuccess) return st;
-  permute_kernel<<<static_cast<unsigned>(p.grid), kPermuteThreads, p.smem, stream>>>(a, p);
+  st = launch_pdl(permute_kernel, dim3(static_cast<unsigned>(p.grid)), dim3(kPermuteThreads), p.smem, stream, a, p);
+  if (st != cudaSuccess) return st;
   count_launch();
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace moe

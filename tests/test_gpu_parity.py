@@ -44,8 +44,8 @@ def bf16_bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
 
 
-def run_gpu_layout(w, idx_cpu, cap):
-    lay = binding.Layout(w, cap, device=DEV).build(idx_cpu.to(DEV))
+def run_gpu_layout(w, idx_cpu, cap, fused=True):
+    lay = binding.Layout(w, cap, device=DEV).build(idx_cpu.to(DEV), fused=fused)
     return lay
 
 
@@ -78,14 +78,14 @@ def check_combine(got_bits: np.ndarray, want_bits: np.ndarray):
     np.testing.assert_array_equal(got_bits, want_bits)
 
 
-def full_case(w: wl.Workload, seed: int, combine=True, cap=None):
+def full_case(w: wl.Workload, seed: int, combine=True, cap=None, fused=True):
     """Everything compared whole against the oracle (sizes the host can hold twice)."""
     inp = wl.make(w, seed)
     idx = inp["topk_idx"]
     cap = cap if cap is not None else wl.worst_case_rows(w)
     ref = oracle.layout(idx.numpy(), w.num_experts, w.num_ranks, w.alignment, capacity_rows=cap)
     assert ref["status"] == oracle.OK
-    lay = run_gpu_layout(w, idx, cap)
+    lay = run_gpu_layout(w, idx, cap, fused=fused)
     rows = ref["total_rows"]
     x = inp["x"].to(DEV)
     recv = torch.full((cap, w.hidden), 0x5A, dtype=torch.uint8, device=DEV).view(x.dtype) \
@@ -116,10 +116,11 @@ def full_case(w: wl.Workload, seed: int, combine=True, cap=None):
 
 
 # ------------------------------------------------------- workload parity
+@pytest.mark.parametrize("fused", [True, False], ids=["one_call", "two_calls"])
 @pytest.mark.parametrize("name", ["tiny", "decode", "skewed", "prefill_fp8"])
-def test_workload_full_parity(name):
+def test_workload_full_parity(name, fused):
     w = wl.WORKLOADS[name]
-    full_case(w, wl.SEEDS[name])
+    full_case(w, wl.SEEDS[name], fused=fused)
 
 
 def test_roundtrip_full_size():
@@ -191,17 +192,30 @@ EDGE = [
 ]
 
 
+@pytest.mark.parametrize("fused", [True, False], ids=["one_call", "two_calls"])
 @pytest.mark.parametrize("w", EDGE, ids=lambda w: f"N{w.num_tokens}_K{w.topk}_E{w.num_experts}_A{w.alignment}")
-def test_edge_parity(w):
-    full_case(w, seed=123)
+def test_edge_parity(w, fused):
+    full_case(w, seed=123, fused=fused)
+
+
+def test_more_tiles_than_fit_at_once():
+    """200000 tokens at top-32 make more tiles than can be resident: the one-call
+    path falls back to the separate kernels and must give the same layout."""
+    w = _w(200000, 32, 64, 4, 16, H=16)
+    idx = wl.draw_topk_idx(w, 31)
+    ref = oracle.layout(idx.numpy(), 64, 4, 16)
+    for fused in (True, False):
+        lay = run_gpu_layout(w, idx, wl.worst_case_rows(w), fused=fused)
+        assert lay.error() == 0
+        assert_layout_matches(lay, ref, w)
 
 
 def test_empty_and_all_masked():
-    for N in (0, 100):
+    for N, fused in ((0, True), (0, False), (100, True), (100, False)):
         w = _w(N, 4, 16, 4, 8)
         idx = torch.full((N, 4), -1, dtype=torch.int64)
         ref = oracle.layout(idx.numpy(), 16, 4, 8)
-        lay = run_gpu_layout(w, idx, 64)
+        lay = run_gpu_layout(w, idx, 64, fused=fused)
         x = torch.randn(N, 64, device=DEV).to(torch.bfloat16)
         recv = torch.full((64, 64), 3.0, dtype=torch.bfloat16, device=DEV)
         lay.permute(x, recv)
@@ -228,10 +242,13 @@ def test_capacity_error_is_reported_and_nothing_written():
     inp = wl.make(w, 5)
     ref = oracle.layout(inp["topk_idx"].numpy(), 32, 4, 16)
     cap = ref["total_rows"] - 1
-    lay = binding.Layout(w, cap, device=DEV)
-    lay.src_idx.fill_(-5)
-    lay.build(inp["topk_idx"].to(DEV))
-    assert lay.error() == 4
+    for fused in (True, False):
+        lay = binding.Layout(w, cap, device=DEV)
+        lay.src_idx.fill_(-5)
+        lay.build(inp["topk_idx"].to(DEV), fused=fused)
+        assert lay.error() == 4
+        assert torch.all(lay.dst_slot == -1) and torch.all(lay.src_idx == -5)
+    assert lay.error() == 0
     assert int(lay.total_rows.item()) == ref["total_rows"]
     np.testing.assert_array_equal(lay.expert_offset.cpu().numpy(), ref["expert_offset"])
     assert torch.all(lay.dst_slot == -1) and torch.all(lay.src_idx == -5)
@@ -248,9 +265,10 @@ def test_bad_expert_id_is_reported_and_dropped():
     idx[10, 0] = 1 << 40
     ref = oracle.layout(idx.numpy(), 16, 4, 4)
     assert ref["status"] == oracle.BAD_EXPERT_ID
-    lay = run_gpu_layout(w, idx, wl.worst_case_rows(w))
-    assert lay.error() == 3
-    assert_layout_matches(lay, ref, w)
+    for fused in (True, False):
+        lay = run_gpu_layout(w, idx, wl.worst_case_rows(w), fused=fused)
+        assert lay.error() == 3
+        assert_layout_matches(lay, ref, w)
 
 
 def test_zero_pad_off_leaves_gap_rows():
@@ -301,5 +319,8 @@ def test_combine_k32_and_out_of_range_slot():
 
 def test_kernel_launch_counter_moves():
     before = binding.kernel_launches()
-    full_case(wl.WORKLOADS["tiny"], 0)
-    assert binding.kernel_launches() - before == 5
+    full_case(wl.WORKLOADS["tiny"], 0, fused=False)
+    assert binding.kernel_launches() - before == 5     # count, column scan, rank, permute, combine
+    before = binding.kernel_launches()
+    full_case(wl.WORKLOADS["tiny"], 0, fused=True)
+    assert binding.kernel_launches() - before == 3     # fused layout, permute, combine
