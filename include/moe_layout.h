@@ -176,6 +176,38 @@ MOE_API int moe_combine_unpermute(const moe_layout_desc* desc, const void* exper
                           void* stream);
 
 /*
+ * moe_layout_build without a caller workspace, for callers that cannot
+ * allocate device memory when they build the layout: for example an engine
+ * that reserves all of HBM for its own allocator at start-up and forbids
+ * cudaMalloc afterwards, a plugin that must not touch its host's memory
+ * pool, or a latency-critical loop that cannot afford cudaMalloc's implicit
+ * device synchronisation.  The pages have no counterpart to this call; it
+ * exists only for such callers.
+ *
+ * Inputs and outputs are the caller's, exactly as for moe_layout_build.  The
+ * scratch is a fixed array of MOE_NOALLOC_SCRATCH_BYTES inside the library,
+ * which every GPU that loads the library holds until the process exits.
+ *  - Problems whose workspace (moe_layout_workspace_bytes) is larger than
+ *    that are rejected with MOE_ERR_UNSUPPORTED before anything is launched.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - Every call on a device shares the array.  Each call clears the parts
+ *    that must start at zero, but calls that overlap on the GPU (different
+ *    streams, no ordering between them) race on it and give wrong results.
+ *  - device_error: device int32 [1] that receives this call's device-side
+ *    status (MOE_OK, MOE_ERR_BAD_EXPERT_ID, MOE_ERR_CAPACITY, MOE_ERR_TIMEOUT),
+ *    written on `stream` after the layout.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
+MOE_API int moe_layout_build_noalloc(const moe_layout_desc* desc, const int64_t* topk_idx,
+                                     int32_t* expert_count, int32_t* rank_count,
+                                     int32_t* expert_offset, int32_t* rank_psum,
+                                     int32_t* dst_slot, int32_t* src_idx, int64_t capacity_rows,
+                                     int32_t* total_rows, int32_t* device_error, void* stream);
+
+/*
  * Synchronise `stream`, copy the workspace's sticky error word (the first
  * device-side error since the last read; MOE_OK if none) into
  * *device_error, and reset it to MOE_OK.
