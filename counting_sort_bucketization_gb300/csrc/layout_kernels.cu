@@ -116,6 +116,8 @@ __device__ void count_phase(const TilePlan& plan, int K, int E, int R, int tile,
 // Expert rows become exclusive prefixes over tiles and give expert_count;
 // rank rows give rank_count.  Loads go through L2 (__ldcg): in the fused
 // kernel other CTAs wrote these rows earlier in the same launch.
+constexpr int kScanRegChunks = 8;   // rows of up to 8 x 32 tiles are scanned from registers
+
 __device__ void scan_phase(int32_t* __restrict__ hist, const int32_t* __restrict__ rhist, int64_t T, int E,
                            int R, int32_t* __restrict__ expert_count, int32_t* __restrict__ rank_count) {
   const int warp = threadIdx.x / kWarpSize, lane = threadIdx.x % kWarpSize;
@@ -125,6 +127,35 @@ __device__ void scan_phase(int32_t* __restrict__ hist, const int32_t* __restrict
     const bool is_expert = row < E;
     const int32_t* src = is_expert ? hist + static_cast<int64_t>(row) * T
                                    : rhist + static_cast<int64_t>(row - E) * T;
+    if (T <= kWarpSize * kScanRegChunks) {
+      // All loads first (coalesced, 32 tiles per load), then one warp scan per
+      // 32-tile chunk with a running carry: one L2 round trip per row.
+      int v[kScanRegChunks];
+#pragma unroll
+      for (int j = 0; j < kScanRegChunks; ++j) {
+        const int64_t i = j * kWarpSize + lane;
+        v[j] = i < T ? __ldcg(src + i) : 0;
+      }
+      int carry = 0;
+      int32_t* dst = is_expert ? hist + static_cast<int64_t>(row) * T : nullptr;
+#pragma unroll
+      for (int j = 0; j < kScanRegChunks; ++j) {
+        if (j * kWarpSize >= T) break;
+        const int incl = warp_inclusive_scan(v[j], lane);
+        const int64_t i = j * kWarpSize + lane;
+        if (is_expert && i < T) dst[i] = carry + incl - v[j];
+        carry += __shfl_sync(kFull, incl, kWarpSize - 1);
+      }
+      if (lane == 0) {
+        if (is_expert)
+          expert_count[row] = carry;
+        else
+          rank_count[row - E] = carry;
+      }
+      continue;
+    }
+    // Longer rows: each lane sums a contiguous run, warp scan of the run sums,
+    // then each lane rewrites its run.
     int sum = 0;
     for (int64_t i = lo; i < hi; ++i) sum += __ldcg(src + i);
     const int incl = warp_inclusive_scan(sum, lane);
@@ -169,26 +200,38 @@ __device__ void rank_phase(const TilePlan& plan, const RankArgs& a, int tile, Ti
   const int npairs = tc.ntok * K;
   const int warp = threadIdx.x / kWarpSize, lane = threadIdx.x % kWarpSize;
 
-  // Aligned exclusive sum over experts ([CS] §7.2 then §5.5), block-wide.
-  // Thread i owns experts [i*ipt, (i+1)*ipt).
+  // Both global reads of this phase are issued up front, so their latencies
+  // overlap: the aligned counts of this thread's experts [i*ipt, (i+1)*ipt)
+  // and this tile's earlier-tile counts for experts tid, tid+256, ...
+  // (E <= MOE_MAX_EXPERTS = 4 * kLayoutThreads).
+  constexpr int kPerThread = MOE_MAX_EXPERTS / kLayoutThreads;
   const int ipt = static_cast<int>(ceil_div64(E, kLayoutThreads));
   const int e_lo = threadIdx.x * ipt;
-  int mine = 0;
-  for (int j = 0; j < ipt; ++j) {
+  int aligned[kPerThread], prior[kPerThread];
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) {
     const int e = e_lo + j;
-    if (e < E) mine += static_cast<int>(ceil_div64(__ldcg(a.expert_count + e), A) * A);
+    aligned[j] = (j < ipt && e < E) ? static_cast<int>(ceil_div64(__ldcg(a.expert_count + e), A) * A) : 0;
+    const int e2 = threadIdx.x + j * kLayoutThreads;
+    prior[j] = (e2 < E && tile < T) ? __ldcg(a.hist_prefix + static_cast<int64_t>(e2) * T + tile) : 0;
   }
+
+  // Aligned exclusive sum over experts ([CS] §7.2 then §5.5), block-wide.
+  int mine = 0;
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) mine += aligned[j];
   const int incl = warp_inclusive_scan(mine, lane);
   if (lane == kWarpSize - 1) warp_tot_s[warp] = incl;
   __syncthreads();
   int warp_base = 0;
   for (int w = 0; w < warp; ++w) warp_base += warp_tot_s[w];
   int run = warp_base + incl - mine;
-  for (int j = 0; j < ipt; ++j) {
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) {
     const int e = e_lo + j;
-    if (e < E) {
+    if (j < ipt && e < E) {
       off_s[e] = run;
-      run += static_cast<int>(ceil_div64(__ldcg(a.expert_count + e), A) * A);
+      run += aligned[j];
     }
   }
   if (threadIdx.x == kLayoutThreads - 1) off_s[E] = run;
@@ -237,12 +280,16 @@ __device__ void rank_phase(const TilePlan& plan, const RankArgs& a, int tile, Ti
   __syncthreads();
 
   // Per expert: turn the per-warp counts into absolute slot bases.
-  for (int e = threadIdx.x; e < E && tile < T; e += blockDim.x) {
-    int b = off_s[e] + __ldcg(a.hist_prefix + static_cast<int64_t>(e) * T + tile);
-    for (int w = 0; w < kLayoutWarps; ++w) {
-      const int c = cnt_s[w * E + e];
-      cnt_s[w * E + e] = b;
-      b += c;
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) {
+    const int e = threadIdx.x + j * kLayoutThreads;
+    if (e < E && tile < T) {
+      int b = off_s[e] + prior[j];
+      for (int w = 0; w < kLayoutWarps; ++w) {
+        const int c = cnt_s[w * E + e];
+        cnt_s[w * E + e] = b;
+        b += c;
+      }
     }
   }
   __syncthreads();

@@ -66,6 +66,8 @@ def _declare(lib: ctypes.CDLL) -> None:
     i32, i64, p = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
     lib.oracle_layout.restype = ctypes.c_int
     lib.oracle_layout.argtypes = [i64, i32, i32, i32, i32, p, p, p, p, p, p, p, i64, p]
+    lib.oracle_rank_layout.restype = ctypes.c_int
+    lib.oracle_rank_layout.argtypes = [i64, i32, i32, i32, p, p, p, i64, p]
     lib.oracle_permute.restype = ctypes.c_int
     lib.oracle_permute.argtypes = [i64, i32, p, p, i64, p, i64, i32, p, p, p, p, i64, i32]
     lib.oracle_f32_to_bf16.restype = None
@@ -115,6 +117,24 @@ def layout(topk_idx, num_experts: int, num_ranks: int, alignment: int,
     rows = int(total.value)
     return dict(status=int(st), expert_count=ec, rank_count=rc, expert_offset=off, rank_psum=rps,
                 dst_slot=dst, src_idx=src[:rows] if st != CAPACITY else src, total_rows=rows)
+
+
+def rank_layout(topk_idx, num_experts: int, num_ranks: int, capacity_rows: int | None = None,
+                lib: ctypes.CDLL | None = None) -> dict:
+    """Non-expand (rank-contiguous) slot map: ``status``, ``rank_slot`` [N, K],
+    ``rank_src`` [rows], ``total_rows``."""
+    lib = lib or load()
+    idx = _as(topk_idx, np.int64)
+    N, K = idx.shape
+    if capacity_rows is None:
+        capacity_rows = N * num_ranks
+    slot = np.full((N, K), -1, np.int32)
+    src = np.full(max(int(capacity_rows), 0), -1, np.int32)
+    total = ctypes.c_int64(0)
+    st = lib.oracle_rank_layout(N, K, int(num_experts), int(num_ranks), _ptr(idx), _ptr(slot), _ptr(src),
+                                int(capacity_rows), ctypes.addressof(total))
+    rows = int(total.value)
+    return dict(status=int(st), rank_slot=slot, rank_src=src[:rows] if st != CAPACITY else src, total_rows=rows)
 
 
 def permute(x_bytes: np.ndarray, dst_slot, expert_offset, expert_count, rows: int,

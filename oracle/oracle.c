@@ -131,6 +131,75 @@ int oracle_layout(int64_t N, int32_t K, int32_t E, int32_t R, int32_t A,
 }
 
 /*
+ * oracle_rank_layout -- the non-expand (rank-contiguous) slot map
+ * ([CS] §6.2 "Scatter 1", §8.1-§8.2).
+ *
+ * Each token is copied once per logical rank it reaches (deduplicated, as
+ * in the count of [CS] §4.2).  Rank r's block of rows starts at the
+ * exclusive sum of rank_count over earlier ranks; inside it tokens are in
+ * ascending order (the page hands out these slots with an atomic counter,
+ * so any order is valid for it).  Of the token's top-k slots that reach
+ * rank r, the highest k (the page's "master lane", the highest lane of the
+ * group) gets the row; the others, and masked slots, get -1.
+ *   rank_slot[t*K+k]: row in the rank-contiguous buffer or -1;
+ *   rank_src[row]:    token of each row ([rows], rows = sum of rank_count).
+ * Ids >= E are dropped as in oracle_layout.  Returns ORACLE_CAPACITY if the
+ * rows exceed capacity_rows (maps untouched), ORACLE_BAD_EXPERT_ID if a bad
+ * id was seen.
+ */
+int oracle_rank_layout(int64_t N, int32_t K, int32_t E, int32_t R,
+                       const int64_t *topk_idx, int32_t *rank_slot,
+                       int32_t *rank_src, int64_t capacity_rows,
+                       int64_t *total_rows) {
+  if (N < 0 || K < 1 || E < 1 || R < 1 || E % R != 0) return ORACLE_BAD_ARG;
+  const int32_t L = E / R;
+  int status = ORACLE_OK;
+  /* Rank counts, one per token per rank ([CS] §4.2). */
+  int64_t *count = (int64_t *)calloc((size_t)R, sizeof(int64_t));
+  int64_t *last_token = (int64_t *)malloc(sizeof(int64_t) * (size_t)R);
+  if (!count || !last_token) return ORACLE_BAD_ARG;
+  for (int32_t r = 0; r < R; ++r) last_token[r] = -1;
+  for (int64_t t = 0; t < N; ++t) {
+    for (int32_t k = 0; k < K; ++k) {
+      int64_t e = topk_idx[t * K + k];
+      if (e < 0) continue;
+      if (e >= E) { status = ORACLE_BAD_EXPERT_ID; continue; }
+      int32_t r = (int32_t)(e / L);
+      if (last_token[r] != t) { last_token[r] = t; count[r] += 1; }
+    }
+  }
+  /* Exclusive sum over ranks: the start of each rank's block. */
+  int64_t *cursor = (int64_t *)malloc(sizeof(int64_t) * (size_t)R);
+  if (!cursor) return ORACLE_BAD_ARG;
+  int64_t run = 0;
+  for (int32_t r = 0; r < R; ++r) { cursor[r] = run; run += count[r]; }
+  *total_rows = run;
+  free(count);
+  if (run > capacity_rows) { free(last_token); free(cursor); return ORACLE_CAPACITY; }
+  /* Scatter: tokens in order; the highest k reaching rank r takes the row. */
+  for (int64_t t = 0; t < N; ++t) {
+    for (int32_t k = 0; k < K; ++k) rank_slot[t * K + k] = -1;
+    for (int32_t k = K - 1; k >= 0; --k) {
+      int64_t e = topk_idx[t * K + k];
+      if (e < 0 || e >= E) continue;
+      int32_t r = (int32_t)(e / L);
+      int taken = 0;
+      for (int32_t k2 = k + 1; k2 < K; ++k2) {
+        int64_t e2 = topk_idx[t * K + k2];
+        if (e2 >= 0 && e2 < E && (int32_t)(e2 / L) == r) { taken = 1; break; }
+      }
+      if (taken) continue;
+      rank_slot[t * K + k] = (int32_t)cursor[r];
+      rank_src[cursor[r]] = (int32_t)t;
+      cursor[r] += 1;
+    }
+  }
+  free(last_token);
+  free(cursor);
+  return status;
+}
+
+/*
  * oracle_permute -- the expand-mode row scatter ([CS] §6.4, §8.2) and the
  * zero padding of the alignment gap ([CS] §7.3).
  *

@@ -27,6 +27,9 @@ What pins what (page: "07 DeepEP Counting Sort / Bucketization", sections):
                     from x that never builds the receive buffer.
   bf16           -- fp32 -> bf16 rounding vs. torch's CPU cast.
   errors         -- bad expert ids and too-small capacity are reported.
+  rank_sort      -- the non-expand (rank-contiguous) rows as a library sort of the
+                    distinct (token, rank) pairs; master lane = highest k (§6.2);
+                    also part of handworked and bruteforce.
 """
 from __future__ import annotations
 
@@ -103,6 +106,29 @@ def sort_formulation(idx: np.ndarray, E: int, R: int, A: int) -> dict:
                 total_rows=int(offsets[-1]))
 
 
+def rank_sort_formulation(idx: np.ndarray, E: int, R: int) -> dict:
+    """Non-expand rows as a sort of the distinct (token, rank) pairs by (rank, token);
+    the row goes to the highest k of the token that reaches the rank."""
+    N, K = idx.shape
+    L = E // R
+    flat = idx.reshape(-1)
+    pairs = np.nonzero(flat >= 0)[0]
+    t_of, r_of, k_of = pairs // K, flat[pairs] // L, pairs % K
+    key = t_of * R + r_of
+    uniq = np.unique(key)                                  # (t, r) pairs, t-major
+    ut, ur = uniq // R, uniq % R
+    order = np.lexsort((ut, ur))                           # by rank, then token
+    row_of = np.empty(uniq.size, np.int64)
+    row_of[order] = np.arange(uniq.size)
+    master_k = np.full(uniq.size, -1)
+    np.maximum.at(master_k, np.searchsorted(uniq, key), k_of)
+    slot = np.full((N, K), -1, np.int64)
+    slot[ut, master_k] = row_of
+    src = np.empty(uniq.size, np.int64)
+    src[row_of] = ut
+    return dict(rank_slot=slot, rank_src=src, total_rows=int(uniq.size))
+
+
 def assert_layout_equal(got: dict, want: dict, ctx=""):
     for key in ("expert_count", "rank_count", "expert_offset", "rank_psum", "dst_slot", "src_idx"):
         np.testing.assert_array_equal(np.asarray(got[key]), np.asarray(want[key]), err_msg=f"{key} {ctx}")
@@ -156,6 +182,10 @@ def check_handworked(lib):
     assert r["status"] == oracle.OK
     assert_layout_equal(r, g, "handworked")
     np.testing.assert_array_equal(r["expert_offset"][:-1] + r["expert_count"], g["handle_psum"])
+    rr = oracle.rank_layout(idx, E, R, lib=lib)
+    assert rr["status"] == oracle.OK and rr["total_rows"] == sum(g["rank_count"])
+    np.testing.assert_array_equal(rr["rank_slot"], g["rank_slot"])
+    np.testing.assert_array_equal(rr["rank_src"], g["rank_src"])
     # rows: token t's row is bf16 values (t+1)/8 .. so n * x is exact
     H = 8
     x = np.zeros((4, H), np.float32)
@@ -224,6 +254,24 @@ def check_sort_formulation(lib, cases=SORT_CASES, seed=11):
         assert_layout_equal(r, sort_formulation(idx, E, R, A), f"case {case}")
 
 
+def check_rank_sort_formulation(lib, cases=SORT_CASES, seed=21):
+    rng = np.random.default_rng(seed)
+    for case in cases:
+        N, K, E, R, A, mask, skew = case
+        idx = random_idx(rng, N, K, E, mask, skew)
+        r = oracle.rank_layout(idx, E, R, lib=lib)
+        want = rank_sort_formulation(idx, E, R)
+        assert r["status"] == oracle.OK and r["total_rows"] == want["total_rows"], case
+        np.testing.assert_array_equal(r["rank_slot"], want["rank_slot"], err_msg=str(case))
+        np.testing.assert_array_equal(r["rank_src"], want["rank_src"], err_msg=str(case))
+        # rank blocks have the expand layout's rank counts, in rank order
+        lay = oracle.layout(idx, E, R, A, lib=lib)
+        starts = np.concatenate([[0], lay["rank_psum"][:-1]])
+        for rr_ in range(R):
+            blk = r["rank_src"][starts[rr_]:lay["rank_psum"][rr_]]
+            assert blk.size == lay["rank_count"][rr_] and np.all(np.diff(blk) > 0)
+
+
 def check_invariants(lib, seed=12):
     rng = np.random.default_rng(seed)
     for case in SORT_CASES:
@@ -257,8 +305,22 @@ def _definition_by_enumeration(idx, E, R, A):
                          if (t2, k2) < (t, k) and idx[t2, k2] == e)
             dst[t, k] = off[e] + before
             src[off[e] + before] = t
+    # non-expand rows: (t, r) pairs by rank then token; the highest k reaching r takes the row
+    rstart = [sum(rc[:r]) for r in range(R)]
+    rslot = np.full((N, K), -1, np.int64)
+    rsrc = np.full(sum(rc), -1, np.int64)
+    for t in range(N):
+        for r in range(R):
+            ks = [k for k in range(K) if idx[t, k] >= 0 and idx[t, k] // L == r]
+            if not ks:
+                continue
+            row = rstart[r] + sum(1 for t2 in range(t) if any(idx[t2, k] >= 0 and idx[t2, k] // L == r
+                                                              for k in range(K)))
+            rslot[t, max(ks)] = row
+            rsrc[row] = t
     return dict(expert_count=cnt, rank_count=rc, expert_offset=off,
-                rank_psum=np.cumsum(rc), dst_slot=dst, src_idx=src, total_rows=off[E])
+                rank_psum=np.cumsum(rc), dst_slot=dst, src_idx=src, total_rows=off[E],
+                rank_slot=rslot, rank_src=rsrc)
 
 
 BRUTE_SHAPES = [(1, 1, 3), (2, 2, 3), (3, 2, 2), (1, 3, 4), (2, 1, 4)]
@@ -273,8 +335,12 @@ def check_bruteforce(lib, shapes=BRUTE_SHAPES, alignments=(1, 2, 3)):
                 for A in alignments:
                     r = oracle.layout(idx, E, R, A, lib=lib)
                     assert r["status"] == oracle.OK
-                    assert_layout_equal(r, _definition_by_enumeration(idx, E, R, A),
-                                        f"idx={combo} E={E} R={R} A={A}")
+                    want = _definition_by_enumeration(idx, E, R, A)
+                    assert_layout_equal(r, want, f"idx={combo} E={E} R={R} A={A}")
+                    if A == 1:
+                        rr = oracle.rank_layout(idx, E, R, lib=lib)
+                        np.testing.assert_array_equal(rr["rank_slot"], want["rank_slot"])
+                        np.testing.assert_array_equal(rr["rank_src"], want["rank_src"])
 
 
 def check_permute(lib, seed=13):
@@ -494,13 +560,19 @@ def check_errors(lib):
     assert r["status"] == oracle.BAD_EXPERT_ID
     np.testing.assert_array_equal(r["expert_count"], [1, 1, 1, 0])
     np.testing.assert_array_equal(r["dst_slot"], [[0, -1], [2, -1], [-1, 4]])
+    rr = oracle.rank_layout(idx, 4, 2, lib=lib)
+    assert rr["status"] == oracle.BAD_EXPERT_ID
+    np.testing.assert_array_equal(rr["rank_slot"], [[0, -1], [1, -1], [-1, 2]])
     idx = np.array([[0], [0], [0]], np.int64)
     r = oracle.layout(idx, 2, 1, 4, capacity_rows=3, lib=lib)
     assert r["status"] == oracle.CAPACITY and r["total_rows"] == 4
+    rr = oracle.rank_layout(idx, 2, 1, capacity_rows=2, lib=lib)
+    assert rr["status"] == oracle.CAPACITY and rr["total_rows"] == 3
 
 
 ALL_CHECKS = [
-    check_handworked, check_padding_example, check_sort_formulation, check_invariants,
+    check_handworked, check_padding_example, check_sort_formulation, check_rank_sort_formulation,
+    check_invariants,
     check_bruteforce, check_permute, check_combine_closed_form, check_combine_bound,
     check_combine_exact, check_roundtrip_direct, check_bf16, check_errors,
 ]

@@ -21,11 +21,13 @@ MUTATIONS = [
     ("no_alignment", "run += align_up(expert_count[e], A);", "run += expert_count[e];"),
     ("align_rounds_down", "return ((x + a - 1) / a) * a;", "return (x / a) * a;"),
     ("align_one_too_many", "return ((x + a - 1) / a) * a;", "return ((x + a) / a) * a;"),
-    ("no_rank_dedup", "if (last_token[r] != t) {", "if (1) {"),
-    ("rank_is_e_mod_R", "int32_t r = (int32_t)(e / L);", "int32_t r = (int32_t)(e % R);"),
+    ("no_rank_dedup", "if (last_token[r] != t) {\n        last_token[r] = t;", "if (1) {\n        last_token[r] = t;"),
+    ("rank_is_e_mod_R", "expert_count[e] += 1;\n      int32_t r = (int32_t)(e / L);",
+     "expert_count[e] += 1;\n      int32_t r = (int32_t)(e % R);"),
     ("rank_psum_exclusive", "rrun += rank_count[r];\n    rank_psum[r] = (int32_t)rrun;",
      "rank_psum[r] = (int32_t)rrun;\n    rrun += rank_count[r];"),
-    ("expert_zero_dropped", "if (e < 0) continue;", "if (e <= 0) continue;"),
+    ("expert_zero_dropped", "if (e < 0) continue;\n      if (e >= E) { status = ORACLE_BAD_EXPERT_ID; continue; }\n      expert_count",
+     "if (e <= 0) continue;\n      if (e >= E) { status = ORACLE_BAD_EXPERT_ID; continue; }\n      expert_count"),
     ("pads_first_in_segment", "cursor[e] = expert_offset[e];",
      "cursor[e] = expert_offset[e + 1] - expert_count[e];"),
     ("token_order_reversed",
@@ -44,6 +46,11 @@ MUTATIONS = [
     ("bf16_truncates", "u += 0x7fffu + keep_lsb;", "u += 0u * keep_lsb;"),
     ("bf16_ties_away", "u += 0x7fffu + keep_lsb;", "u += 0x8000u + 0u * keep_lsb;"),
     ("expert_scale_wrong_expert", "* scale[e]);", "* scale[e == 0 ? 0 : e - 1]);"),
+    ("rank_rows_to_lowest_lane", "for (int32_t k2 = k + 1; k2 < K; ++k2) {", "for (int32_t k2 = 0; k2 < k; ++k2) {"),
+    ("rank_rows_dedup_ignored_in_count", "if (last_token[r] != t) { last_token[r] = t; count[r] += 1; }",
+     "count[r] += 1;"),
+    ("rank_rows_no_dedup", "if (taken) continue;", "(void)taken;"),
+    ("rank_block_start_inclusive", "cursor[r] = run; run += count[r];", "run += count[r]; cursor[r] = run - 1;"),
 ]
 
 
