@@ -41,8 +41,8 @@ L2_FLUSH_BYTES = 256 << 20          # > 2x the 129 MB L2
 # DRAM traffic of the permute kernel from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), per launch, scaled to the decode workload, tied to
 # the kernel sources it was measured on.  bench reports null if they changed.
-PERMUTE_TRAFFIC = {"sha256": "20590e636ba8c913fa638a7cb2a6c6841bdc0eb8684fbb28067745f579023a27",
-                   "workload": "decode", "bytes_per_launch": 58_903_552 + 646_494_976}
+PERMUTE_TRAFFIC = {"sha256": "82ea9003edeb54802d788183e1902ed93f73deb938f61a48206bdbea331f877e",
+                   "workload": "decode", "bytes_per_launch": 58_980_352 + 646_405_888}
 PERMUTE_SOURCES = ["counting_sort_bucketization_gb300/csrc/permute_kernel.cu",
                    "counting_sort_bucketization_gb300/csrc/ptx.cuh",
                    "counting_sort_bucketization_gb300/csrc/common.cuh"]

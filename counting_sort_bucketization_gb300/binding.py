@@ -74,6 +74,8 @@ def load_library() -> ctypes.CDLL:
         lib.moe_layout_scan.argtypes = [dp, p, p, p, p, sz, p, p, p, p, i64, p, p]
         lib.moe_layout_build.argtypes = [dp, p, p, p, p, sz, p, p, p, p, i64, p, p]
         lib.moe_dispatch_permute.argtypes = [dp, p, i64, p, i64, p, p, p, p, p, i64, ctypes.c_int, p, sz, p]
+        lib.moe_layout_rank_rows.argtypes = [dp, p, p, p, sz, p, p, i64, p]
+        lib.moe_dispatch_permute_ranks.argtypes = [dp, p, i64, p, i64, p, p, p, p, i64, p, sz, p]
         lib.moe_combine_unpermute.argtypes = [dp, p, i64, i64, p, p, p, p, sz, p]
         lib.moe_layout_get_error.argtypes = [p, ctypes.POINTER(i32), p]
         lib.moe_strerror.argtypes = [ctypes.c_int]
@@ -81,6 +83,7 @@ def load_library() -> ctypes.CDLL:
         lib.moe_kernel_launches.argtypes = []
         lib.moe_kernel_launches.restype = ctypes.c_uint64
         for name in ("moe_layout_workspace_bytes", "moe_layout_count", "moe_layout_scan", "moe_layout_build",
+                     "moe_layout_rank_rows", "moe_dispatch_permute_ranks",
                      "moe_dispatch_permute", "moe_combine_unpermute", "moe_layout_get_error"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -202,6 +205,38 @@ def dispatch_permute(desc, x, dst_slot, expert_offset, expert_count, recv_x, wor
     _check(st, "moe_dispatch_permute")
 
 
+def layout_rank_rows(desc, topk_idx, rank_count, workspace, rank_slot, rank_src, stream=None) -> None:
+    """Non-expand slot map (one row per token and rank); follows a layout build on ``workspace``."""
+    N, K, R = int(desc.num_tokens), int(desc.topk), int(desc.num_ranks)
+    st = load_library().moe_layout_rank_rows(
+        ctypes.byref(_desc(desc)), _dev(topk_idx, "topk_idx", torch.int64, N * K),
+        _dev(rank_count, "rank_count", torch.int32, R), _dev(workspace, "workspace", torch.uint8),
+        workspace.numel(), _dev(rank_slot, "rank_slot", torch.int32, N * K), _dev(rank_src, "rank_src", torch.int32),
+        rank_src.numel(), _stream(stream))
+    _check(st, "moe_layout_rank_rows")
+
+
+def dispatch_permute_ranks(desc, x, rank_slot, rank_psum, recv, workspace, sf=None, recv_sf=None,
+                           stream=None) -> None:
+    """recv[rank_slot[t,k]] = x[t] (bytes) for the slots that hold a row; no padding."""
+    N, K, R = int(desc.num_tokens), int(desc.topk), int(desc.num_ranks)
+    cap = recv.shape[0]
+    rb = x.shape[1] * x.element_size()
+    if recv.numel() * recv.element_size() != cap * rb:
+        raise ValueError("recv rows must have the same byte size as x rows")
+    srb = 0
+    if sf is not None:
+        srb = sf.shape[1] * sf.element_size()
+        if recv_sf is None or recv_sf.shape[0] != cap or recv_sf.numel() * recv_sf.element_size() != cap * srb:
+            raise ValueError("recv_sf must be [capacity, sf row] when sf is given")
+    st = load_library().moe_dispatch_permute_ranks(
+        ctypes.byref(_desc(desc)), _dev(x, "x"), rb, _dev(sf, "sf", allow_none=True), srb,
+        _dev(rank_slot, "rank_slot", torch.int32, N * K), _dev(rank_psum, "rank_psum", torch.int32, R),
+        _dev(recv, "recv"), _dev(recv_sf, "recv_sf", allow_none=True), cap,
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    _check(st, "moe_dispatch_permute_ranks")
+
+
 def combine_unpermute(desc, expert_out, dst_slot, weights, out, workspace, stream=None) -> None:
     """out[t] = bf16(sum_k w[t,k] * expert_out[dst_slot[t,k]]) with an fp32 fma chain."""
     N, K = int(desc.num_tokens), int(desc.topk)
@@ -262,6 +297,21 @@ class Layout:
     def permute(self, x, recv_x, sf=None, recv_sf=None, zero_pad=True, stream=None):
         dispatch_permute(self.desc, x, self.dst_slot, self.expert_offset, self.expert_count, recv_x,
                          self.workspace, sf, recv_sf, zero_pad, stream)
+
+    def rank_rows(self, topk_idx, capacity_rows=None, stream=None):
+        """Non-expand slot map after ``build``: sets ``rank_slot`` [N*K] and ``rank_src`` [capacity]."""
+        N, K, R = int(self.desc.num_tokens), int(self.desc.topk), int(self.desc.num_ranks)
+        cap = N * R if capacity_rows is None else int(capacity_rows)
+        dev = self.dst_slot.device
+        self.rank_slot = torch.empty(max(N * K, 1), dtype=torch.int32, device=dev)
+        self.rank_src = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)[:cap]
+        layout_rank_rows(self.desc, topk_idx, self.rank_count, self.workspace, self.rank_slot, self.rank_src,
+                         stream)
+        return self
+
+    def permute_ranks(self, x, recv, sf=None, recv_sf=None, stream=None):
+        dispatch_permute_ranks(self.desc, x, self.rank_slot, self.rank_psum, recv, self.workspace, sf, recv_sf,
+                               stream)
 
     def combine(self, expert_out, weights, out, stream=None):
         combine_unpermute(self.desc, expert_out, self.dst_slot, weights, out, self.workspace, stream)

@@ -32,13 +32,19 @@ cudaError_t launch_build(const moe_layout_desc& d, const TilePlan& p, const int6
                          int32_t* src_idx, int64_t capacity, int32_t* total_rows, int* err,
                          cudaStream_t stream);
 
+// rank_rows_kernel: the non-expand (rank-contiguous) slot map.
+cudaError_t launch_rank_rows(const moe_layout_desc& d, const TilePlan& p, const int64_t* topk_idx,
+                             const int32_t* rhist_prefix, const int32_t* rank_count, int32_t* rank_slot,
+                             int32_t* rank_src, int64_t capacity, int* err, cudaStream_t stream);
+
 struct PermuteArgs {
   const uint8_t* x;
   const uint8_t* sf;
   int64_t row_bytes;
   int64_t sf_row_bytes;
   const int32_t* dst_slot;
-  const int32_t* expert_offset;
+  const int32_t* total_rows;     // rows the layout uses (checked against capacity)
+  const int32_t* expert_offset;  // gap rows (zero_pad only)
   const int32_t* expert_count;
   uint8_t* recv_x;
   uint8_t* recv_sf;

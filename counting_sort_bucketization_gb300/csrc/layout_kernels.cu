@@ -113,12 +113,12 @@ __device__ void count_phase(const TilePlan& plan, int K, int E, int R, int tile,
 
 // ------------------------------------------------- phase: column scan
 // Warp w of CTA b scans rows b*kLayoutWarps + w, + gridDim.x*kLayoutWarps, ...
-// Expert rows become exclusive prefixes over tiles and give expert_count;
-// rank rows give rank_count.  Loads go through L2 (__ldcg): in the fused
+// Every row becomes an exclusive prefix over tiles (in place); expert rows
+// give expert_count, rank rows rank_count.  Loads go through L2 (__ldcg): in the fused
 // kernel other CTAs wrote these rows earlier in the same launch.
 constexpr int kScanRegChunks = 8;   // rows of up to 8 x 32 tiles are scanned from registers
 
-__device__ void scan_phase(int32_t* __restrict__ hist, const int32_t* __restrict__ rhist, int64_t T, int E,
+__device__ void scan_phase(int32_t* __restrict__ hist, int32_t* __restrict__ rhist, int64_t T, int E,
                            int R, int32_t* __restrict__ expert_count, int32_t* __restrict__ rank_count) {
   const int warp = threadIdx.x / kWarpSize, lane = threadIdx.x % kWarpSize;
   const int64_t m = ceil_div64(T, kWarpSize);
@@ -137,13 +137,13 @@ __device__ void scan_phase(int32_t* __restrict__ hist, const int32_t* __restrict
         v[j] = i < T ? __ldcg(src + i) : 0;
       }
       int carry = 0;
-      int32_t* dst = is_expert ? hist + static_cast<int64_t>(row) * T : nullptr;
+      int32_t* dst = const_cast<int32_t*>(src);
 #pragma unroll
       for (int j = 0; j < kScanRegChunks; ++j) {
         if (j * kWarpSize >= T) break;
         const int incl = warp_inclusive_scan(v[j], lane);
         const int64_t i = j * kWarpSize + lane;
-        if (is_expert && i < T) dst[i] = carry + incl - v[j];
+        if (i < T) dst[i] = carry + incl - v[j];
         carry += __shfl_sync(kFull, incl, kWarpSize - 1);
       }
       if (lane == 0) {
@@ -160,17 +160,18 @@ __device__ void scan_phase(int32_t* __restrict__ hist, const int32_t* __restrict
     for (int64_t i = lo; i < hi; ++i) sum += __ldcg(src + i);
     const int incl = warp_inclusive_scan(sum, lane);
     const int total = __shfl_sync(kFull, incl, kWarpSize - 1);
-    if (is_expert) {
-      int32_t* dst = hist + static_cast<int64_t>(row) * T;
-      int run = incl - sum;
-      for (int64_t i = lo; i < hi; ++i) {
-        const int c = __ldcg(dst + i);
-        dst[i] = run;
-        run += c;
-      }
-      if (lane == 0) expert_count[row] = total;
-    } else if (lane == 0) {
-      rank_count[row - E] = total;
+    int32_t* dst = const_cast<int32_t*>(src);
+    int run = incl - sum;
+    for (int64_t i = lo; i < hi; ++i) {
+      const int c = __ldcg(dst + i);
+      dst[i] = run;
+      run += c;
+    }
+    if (lane == 0) {
+      if (is_expert)
+        expert_count[row] = total;
+      else
+        rank_count[row - E] = total;
     }
   }
 }
@@ -334,7 +335,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
 }
 
 __global__ void __launch_bounds__(kLayoutThreads)
-    scan_columns_kernel(int32_t* __restrict__ hist, const int32_t* __restrict__ rhist, int64_t T,
+    scan_columns_kernel(int32_t* __restrict__ hist, int32_t* __restrict__ rhist, int64_t T,
                         int E, int R, int32_t* __restrict__ expert_count,
                         int32_t* __restrict__ rank_count) {
   ptx::grid_dependency_wait();
@@ -415,6 +416,126 @@ __global__ void __launch_bounds__(kLayoutThreads)
   for (int i = threadIdx.x; i < kLayoutWarps * E; i += blockDim.x) cnt_s[i] = 0;
   if (!grid_barrier(bar, bar + 1, gridDim.x, a.err, &flag_s)) return;
   rank_phase(plan, a, blockIdx.x, tc, ids_s, off_s, cnt_s, lr_s, warp_tot_s);
+}
+
+// ------------------------------------------- non-expand rank rows
+// [CS] §6.2 (Scatter 1): one row per (token, rank) the token reaches, in
+// rank r's block [start_r, start_r + rank_count[r]) where start_r is the
+// exclusive sum of rank_count; tokens ascending inside a block.  The row goes
+// to the token's highest k reaching r (the master lane: the highest lane of
+// the __match_any_sync group of that token and rank); the other slots get -1.
+// The slot is start_r + (rows of r in earlier tiles, from the scanned rank
+// histogram) + (rows of r earlier in this tile: match_any + popc among the
+// master lanes, a per-warp running count, a scan over the warps).
+struct RankRowsArgs {
+  int64_t N;
+  int K, E, R;
+  const int32_t* rhist_prefix;   // [R][T] exclusive prefixes over tiles
+  const int32_t* rank_count;
+  int32_t* rank_slot;
+  int32_t* rank_src;
+  int64_t capacity;
+  int* err;
+};
+
+__global__ void __launch_bounds__(kLayoutThreads)
+    rank_rows_kernel(const int64_t* __restrict__ topk_idx, TilePlan plan, RankRowsArgs a) {
+  extern __shared__ int smem[];
+  const int K = a.K, E = a.E, R = a.R, L = E / R;
+  int* start_s = smem;                          // [R+1] block starts, then the total
+  int* cnt_s = start_s + (R + 1);               // [kLayoutWarps][R]
+  int* ids_s = cnt_s + kLayoutWarps * R;        // [tile pairs]
+  int* lr_s = ids_s + plan.tile_tokens * K;     // [tile pairs] rank among masters, -1 otherwise
+  __shared__ int warp_tot_s[kLayoutWarps];
+  const int tile = blockIdx.x;
+  const TileCoords tc = tile_coords(plan, a.N, tile);
+  const int64_t T = plan.tiles;
+  const int warp = threadIdx.x / kWarpSize, lane = threadIdx.x % kWarpSize;
+  for (int i = threadIdx.x; i < kLayoutWarps * R; i += blockDim.x) cnt_s[i] = 0;
+  ptx::grid_dependency_wait();
+  ptx::grid_dependency_launch_dependents();
+  stage_tile_ids(topk_idx, tc.t0 * K, tc.ntok * K, E, ids_s, a.err);
+
+  // Block starts: exclusive sum of rank_count (thread i owns ranks [i*ipt, (i+1)*ipt)).
+  constexpr int kPerThread = MOE_MAX_EXPERTS / kLayoutThreads;
+  const int ipt = static_cast<int>(ceil_div64(R, kLayoutThreads));
+  const int r_lo = threadIdx.x * ipt;
+  int cnt[kPerThread], prior[kPerThread];
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) {
+    const int r = r_lo + j;
+    cnt[j] = (j < ipt && r < R) ? __ldcg(a.rank_count + r) : 0;
+    const int r2 = threadIdx.x + j * kLayoutThreads;
+    prior[j] = (r2 < R && tile < T) ? __ldcg(a.rhist_prefix + static_cast<int64_t>(r2) * T + tile) : 0;
+  }
+  int mine = 0;
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) mine += cnt[j];
+  const int incl = warp_inclusive_scan(mine, lane);
+  if (lane == kWarpSize - 1) warp_tot_s[warp] = incl;
+  __syncthreads();
+  int run = incl - mine;
+  for (int w = 0; w < warp; ++w) run += warp_tot_s[w];
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) {
+    const int r = r_lo + j;
+    if (j < ipt && r < R) {
+      start_s[r] = run;
+      run += cnt[j];
+    }
+  }
+  if (threadIdx.x == kLayoutThreads - 1) start_s[R] = run;
+  __syncthreads();
+  const bool cap_ok = start_s[R] <= a.capacity;
+  if (tile == 0 && threadIdx.x == 0 && !cap_ok) set_error(a.err, MOE_ERR_CAPACITY);
+
+  const int tok_in_chunk = lane / K;
+  int* my_cnt = cnt_s + warp * R;
+  for (int c = 0; c < plan.cpw; ++c) {
+    const int chunk = warp * plan.cpw + c;
+    const int tok = chunk * plan.tpc + tok_in_chunk;
+    const bool in = lane < plan.lanes && tok < tc.ntok;
+    const int pair = chunk * plan.lanes + lane;
+    const int e = in ? ids_s[pair] : -1;
+    const bool valid = e >= 0;
+    const int r = valid ? e / L : 0;
+    // Lanes of one token reaching one rank; the highest of them is the master.
+    const unsigned grp = __match_any_sync(kFull, valid ? static_cast<unsigned>(tok_in_chunk * MOE_MAX_EXPERTS + r)
+                                                       : (0x80000000u | lane));
+    const bool master = valid && (31 - __clz(grp)) == lane;
+    // Masters of the same rank, in lane (= token) order.
+    const unsigned peers = __match_any_sync(kFull, master ? static_cast<unsigned>(r) : (0x80000000u | lane));
+    const int base = master ? my_cnt[r] : 0;
+    __syncwarp();
+    if (master && __ffs(peers) - 1 == lane) my_cnt[r] = base + __popc(peers);
+    if (in) lr_s[pair] = master ? base + __popc(peers & ptx::lanemask_lt()) : -1;
+    __syncwarp();
+  }
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) {
+    const int r = threadIdx.x + j * kLayoutThreads;
+    if (r < R && tile < T) {
+      int b = start_s[r] + prior[j];
+      for (int w = 0; w < kLayoutWarps; ++w) {
+        const int c = cnt_s[w * R + r];
+        cnt_s[w * R + r] = b;
+        b += c;
+      }
+    }
+  }
+  __syncthreads();
+  const int pairs_per_warp = plan.cpw * plan.lanes;
+  const int npairs = tc.ntok * K;
+  for (int i = threadIdx.x; i < npairs; i += blockDim.x) {
+    const int e = ids_s[i];
+    int slot = -1;
+    if (e >= 0 && cap_ok && lr_s[i] >= 0) {
+      slot = cnt_s[(i / pairs_per_warp) * R + e / L] + lr_s[i];
+      a.rank_src[slot] = static_cast<int32_t>(tc.t0 + i / K);
+    }
+    a.rank_slot[tc.t0 * K + i] = slot;
+  }
 }
 
 size_t fused_smem_bytes(const moe_layout_desc& d, const TilePlan& p) {
@@ -509,6 +630,34 @@ cudaError_t launch_rank(const moe_layout_desc& d, const TilePlan& p, const int64
   const RankArgs a = rank_args(d, hist_prefix, expert_count, rank_count, expert_offset, rank_psum, dst_slot,
                                src_idx, capacity, total_rows, err);
   st = launch_pdl(rank_maps_kernel, dim3(static_cast<unsigned>(grid)), dim3(kLayoutThreads), smem, stream,
+                  topk_idx, p, a);
+  if (st != cudaSuccess) return st;
+  count_launch();
+  return cudaSuccess;
+}
+
+cudaError_t launch_rank_rows(const moe_layout_desc& d, const TilePlan& p, const int64_t* topk_idx,
+                             const int32_t* rhist_prefix, const int32_t* rank_count, int32_t* rank_slot,
+                             int32_t* rank_src, int64_t capacity, int* err, cudaStream_t stream) {
+  const size_t smem = sizeof(int) * (static_cast<size_t>(d.num_ranks) + 1 +
+                                     static_cast<size_t>(kLayoutWarps) * d.num_ranks +
+                                     2 * static_cast<size_t>(p.tile_tokens) * d.topk);
+  cudaError_t st = cudaFuncSetAttribute(rank_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(smem));
+  if (st != cudaSuccess) return st;
+  RankRowsArgs a;
+  a.N = d.num_tokens;
+  a.K = d.topk;
+  a.E = d.num_experts;
+  a.R = d.num_ranks;
+  a.rhist_prefix = rhist_prefix;
+  a.rank_count = rank_count;
+  a.rank_slot = rank_slot;
+  a.rank_src = rank_src;
+  a.capacity = capacity;
+  a.err = err;
+  const int64_t grid = p.tiles > 0 ? p.tiles : 1;
+  st = launch_pdl(rank_rows_kernel, dim3(static_cast<unsigned>(grid)), dim3(kLayoutThreads), smem, stream,
                   topk_idx, p, a);
   if (st != cudaSuccess) return st;
   count_launch();

@@ -151,6 +151,7 @@ int moe_dispatch_permute(const moe_layout_desc* desc, const void* x, int64_t row
   a.row_bytes = row_bytes;
   a.sf_row_bytes = sf != nullptr ? sf_row_bytes : 0;
   a.dst_slot = dst_slot;
+  a.total_rows = expert_offset + desc->num_experts;
   a.expert_offset = expert_offset;
   a.expert_count = expert_count;
   a.recv_x = static_cast<uint8_t*>(recv_x);
@@ -160,6 +161,59 @@ int moe_dispatch_permute(const moe_layout_desc* desc, const void* x, int64_t row
   a.topk = desc->topk;
   a.num_experts = desc->num_experts;
   a.zero_pad = zero_pad != 0;
+  a.err = at<int>(workspace, w.err_off);
+  return cuda_status(launch_permute(a, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_layout_rank_rows(const moe_layout_desc* desc, const int64_t* topk_idx, const int32_t* rank_count,
+                         void* workspace, size_t workspace_bytes, int32_t* rank_slot, int32_t* rank_src,
+                         int64_t capacity_rows, void* stream) {
+  if (int st = check_desc(desc)) return st;
+  WorkspaceLayout w;
+  if (int st = check_workspace(desc, workspace, workspace_bytes, &w)) return st;
+  const bool has_pairs = desc->num_tokens > 0;
+  if ((has_pairs && (topk_idx == nullptr || rank_slot == nullptr)) || rank_count == nullptr) return MOE_ERR_INVALID_ARG;
+  if (capacity_rows < 0 || (capacity_rows > 0 && rank_src == nullptr)) return MOE_ERR_INVALID_ARG;
+  const TilePlan p = make_tile_plan(desc->num_tokens, desc->topk);
+  return cuda_status(launch_rank_rows(*desc, p, topk_idx, at<int32_t>(workspace, w.rhist_off), rank_count, rank_slot,
+                                      rank_src, capacity_rows, at<int>(workspace, w.err_off),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+int moe_dispatch_permute_ranks(const moe_layout_desc* desc, const void* x, int64_t row_bytes, const void* sf,
+                               int64_t sf_row_bytes, const int32_t* rank_slot, const int32_t* rank_psum,
+                               void* recv, void* recv_sf, int64_t capacity_rows, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  if (int st = check_desc(desc)) return st;
+  WorkspaceLayout w;
+  if (int st = check_workspace(desc, workspace, workspace_bytes, &w)) return st;
+  const bool has_pairs = desc->num_tokens > 0;
+  if (row_bytes <= 0 || row_bytes % 16 != 0 || capacity_rows < 0) return MOE_ERR_INVALID_ARG;
+  if ((has_pairs && (x == nullptr || rank_slot == nullptr)) || rank_psum == nullptr ||
+      (capacity_rows > 0 && recv == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(recv, 16)) return MOE_ERR_INVALID_ARG;
+  if (sf != nullptr) {
+    if (sf_row_bytes <= 0 || sf_row_bytes % 4 != 0 || !aligned(sf, 4) || !aligned(recv_sf, 4) ||
+        (capacity_rows > 0 && recv_sf == nullptr))
+      return MOE_ERR_INVALID_ARG;
+  }
+  PermuteArgs a{};
+  a.x = static_cast<const uint8_t*>(x);
+  a.sf = static_cast<const uint8_t*>(sf);
+  a.row_bytes = row_bytes;
+  a.sf_row_bytes = sf != nullptr ? sf_row_bytes : 0;
+  a.dst_slot = rank_slot;
+  a.total_rows = rank_psum + (desc->num_ranks - 1);
+  a.expert_offset = nullptr;
+  a.expert_count = nullptr;
+  a.recv_x = static_cast<uint8_t*>(recv);
+  a.recv_sf = sf != nullptr ? static_cast<uint8_t*>(recv_sf) : nullptr;
+  a.capacity = capacity_rows;
+  a.num_tokens = desc->num_tokens;
+  a.topk = desc->topk;
+  a.num_experts = desc->num_experts;
+  a.zero_pad = 0;
   a.err = at<int>(workspace, w.err_off);
   return cuda_status(launch_permute(a, static_cast<cudaStream_t>(stream)));
 }

@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kPermuteThreads)
   }
   ptx::grid_dependency_wait();
   ptx::grid_dependency_launch_dependents();
-  const int64_t rows = __ldg(a.expert_offset + E);
+  const int64_t rows = __ldg(a.total_rows);
   if (rows > a.capacity) {
     if (blockIdx.x == 0 && threadIdx.x == 0) set_error(a.err, MOE_ERR_CAPACITY);
     return;

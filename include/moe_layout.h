@@ -157,6 +157,39 @@ MOE_API int moe_dispatch_permute(const moe_layout_desc* desc, const void* x,
                          size_t workspace_bytes, void* stream);
 
 /*
+ * Non-expand (rank-contiguous) slot map: the page's first scatter
+ * ([CS] §6.2, §8.1-§8.2), where each token goes once to every logical rank
+ * it reaches, whatever the number of that rank's experts it picked.  Must
+ * follow moe_layout_build (or moe_layout_count + moe_layout_scan) on the same
+ * topk_idx and workspace; rank_count is that call's output.  Writes
+ *   rank_slot[N*K]: for each token and rank it reaches, the highest k among
+ *                   the token's slots reaching that rank (the page's master
+ *                   lane) gets the row index; every other slot gets -1;
+ *   rank_src[rows]: token of each row.
+ * Rank r's rows are [rank_psum[r] - rank_count[r], rank_psum[r]); tokens are
+ * in ascending order inside it.  rows = rank_psum[R-1].  If rows exceed
+ * capacity_rows, MOE_ERR_CAPACITY is recorded, every rank_slot is -1 and
+ * rank_src is not written.  N*R rows always suffice.
+ */
+MOE_API int moe_layout_rank_rows(const moe_layout_desc* desc, const int64_t* topk_idx,
+                                 const int32_t* rank_count, void* workspace, size_t workspace_bytes,
+                                 int32_t* rank_slot, int32_t* rank_src, int64_t capacity_rows,
+                                 void* stream);
+
+/*
+ * Non-expand dispatch permute ([CS] §6.3, §8.2 "non-expand"): recv row
+ * rank_slot[t*K+k] = x row t for every slot that has a row; scale-factor
+ * rows move alongside when sf is non-NULL.  No padding.  Argument rules as
+ * for moe_dispatch_permute; rank_psum (from the layout) gives the row total
+ * checked against capacity_rows.
+ */
+MOE_API int moe_dispatch_permute_ranks(const moe_layout_desc* desc, const void* x,
+                                       int64_t row_bytes, const void* sf, int64_t sf_row_bytes,
+                                       const int32_t* rank_slot, const int32_t* rank_psum,
+                                       void* recv, void* recv_sf, int64_t capacity_rows,
+                                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Combine: the inverse of the dispatch.  The pages keep the slot map for it
  * ([CS] §6.2) but print no arithmetic; this is the plain definition
  *   out[t, h] = bf16( sum over k = 0..K-1 with dst_slot[t*K+k] >= 0 of
