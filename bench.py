@@ -319,43 +319,40 @@ def run_native(args, rank, world, local):
     value = world * N / (ms_per_step / 1e3)
     dispatch_ms = float(kern_ms[:2].sum())
 
-    # End to end through the public API with host buffers: pinned inputs in,
-    # the combined tokens (and the row total) back, copies inside the timing.
+    # End to end through the public API with host buffers: pinned ids, rows
+    # and weights in, the combined tokens back.  moe_dispatch_from_host and
+    # moe_combine_to_host overlap the copies with the kernels in chunks; the
+    # copies are inside the timed region.
     idx_h = inp["topk_idx"].pin_memory()
     x_h = inp["x"].pin_memory()
     sf_h = inp["sf"].pin_memory() if inp["sf"] is not None else None
     wt_h = inp["weights"].pin_memory()
     out_h = torch.empty((N, H), dtype=torch.bfloat16).pin_memory()
-    rows_h = torch.empty(1, dtype=torch.int32).pin_memory()
     recv_h = None if do_combine else torch.empty((cap, H), dtype=x_d.dtype).pin_memory()
     h2d = idx_h.numel() * 8 + x_h.numel() * x_h.element_size() + wt_h.numel() * 4 + \
         (sf_h.numel() * 4 if sf_h is not None else 0)
-    d2h = (out_h.numel() * 2 if do_combine else recv_h.numel() * recv_h.element_size()) + 4
+    d2h = out_h.numel() * 2 if do_combine else recv_h.numel() * recv_h.element_size()
+    chunk = -(-N // max(1, args.e2e_chunks))
+    copy_stream = torch.cuda.Stream(dev)
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
     e2e_ms = []
     for i in range(e2e_steps + 2):
         flush_l2()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        idx_d.copy_(idx_h, non_blocking=True)
-        x_d.copy_(x_h, non_blocking=True)
-        wt_d.copy_(wt_h, non_blocking=True)
-        if sf_h is not None:
-            sf_d.copy_(sf_h, non_blocking=True)
-        lay.build(idx_d)
-        lay.permute(x_d, recv, sf_d, recv_sf)
+        binding.dispatch_from_host(lay, idx_h, x_h, idx_d, x_d, recv, weights_host=wt_h, weights=wt_d,
+                                   sf_host=sf_h, sf=sf_d, recv_sf=recv_sf, chunk_tokens=chunk,
+                                   copy_stream=copy_stream)
         if do_combine:
-            lay.combine(eo, wt_d, out)
-            out_h.copy_(out, non_blocking=True)
+            binding.combine_to_host(lay, eo, wt_d, out, out_h, chunk_tokens=chunk, copy_stream=copy_stream)
         else:
             recv_h.copy_(recv, non_blocking=True)
-        rows_h.copy_(lay.total_rows, non_blocking=True)
         b.record(stream)
         if i >= 2:
             e2e_ms.append((a, b))
     torch.cuda.synchronize(dev)
     e2e_step_ms = reduce_max(float(np.mean([a.elapsed_time(b) for a, b in e2e_ms])), world, dev)
-    assert int(rows_h.item()) == rows
+    assert lay.error() == 0, "device error in the end-to-end steps"
 
     if rank != 0:
         return
@@ -379,7 +376,8 @@ def run_native(args, rank, world, local):
         "dispatch_tokens_per_s": world * N / (dispatch_ms / 1e3),
         "layout": {"valid_pairs": ab["P"], "rows": ab["rows"], "tokens_routed": ab["tokens_routed"]},
         "e2e": {"value": world * N / (e2e_step_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps, "chunks": args.e2e_chunks,
+                "api": "moe_dispatch_from_host + moe_combine_to_host"},
         "gpu_launches": launches,
         "wall_s_timed_region": t_wall,
         "clocks": sampler.summary() if sampler else None,
@@ -441,6 +439,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=list(wl.WORKLOADS), default="decode")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--e2e-chunks", type=int, default=4, help="token chunks the host copies are split into")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-max-passes", type=int, default=20)
     ap.add_argument("--ref-seconds", type=float, default=90.0)

@@ -75,6 +75,10 @@ def load_library() -> ctypes.CDLL:
         lib.moe_layout_build.argtypes = [dp, p, p, p, p, sz, p, p, p, p, i64, p, p]
         lib.moe_dispatch_permute.argtypes = [dp, p, i64, p, i64, p, p, p, p, p, i64, ctypes.c_int, p, sz, p]
         lib.moe_layout_rank_rows.argtypes = [dp, p, p, p, sz, p, p, i64, p]
+        lib.moe_layout_accumulate_stats.argtypes = [dp, p, p, p]
+        lib.moe_dispatch_from_host.argtypes = [dp, p, p, i64, p, i64, p, p, p, p, p, p, p, p, p, p, p, p, p, p,
+                                               i64, p, sz, i64, p, p]
+        lib.moe_combine_to_host.argtypes = [dp, p, i64, i64, p, p, p, p, p, sz, i64, p, p]
         lib.moe_dispatch_permute_ranks.argtypes = [dp, p, i64, p, i64, p, p, p, p, i64, p, sz, p]
         lib.moe_combine_unpermute.argtypes = [dp, p, i64, i64, p, p, p, p, sz, p]
         lib.moe_layout_get_error.argtypes = [p, ctypes.POINTER(i32), p]
@@ -83,7 +87,8 @@ def load_library() -> ctypes.CDLL:
         lib.moe_kernel_launches.argtypes = []
         lib.moe_kernel_launches.restype = ctypes.c_uint64
         for name in ("moe_layout_workspace_bytes", "moe_layout_count", "moe_layout_scan", "moe_layout_build",
-                     "moe_layout_rank_rows", "moe_dispatch_permute_ranks",
+                     "moe_layout_rank_rows", "moe_dispatch_permute_ranks", "moe_dispatch_from_host",
+                     "moe_combine_to_host", "moe_layout_accumulate_stats",
                      "moe_dispatch_permute", "moe_combine_unpermute", "moe_layout_get_error"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -250,6 +255,70 @@ def combine_unpermute(desc, expert_out, dst_slot, weights, out, workspace, strea
         _dev(dst_slot, "dst_slot", torch.int32, N * K), _dev(weights, "weights", torch.float32, N * K),
         _dev(out, "out"), _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
     _check(st, "moe_combine_unpermute")
+
+
+def accumulate_stats(desc, expert_count, cumulative, stream=None) -> None:
+    """cumulative[e] += expert_count[e] on the device (int64 running totals)."""
+    E = int(desc.num_experts)
+    st = load_library().moe_layout_accumulate_stats(
+        ctypes.byref(_desc(desc)), _dev(expert_count, "expert_count", torch.int32, E),
+        _dev(cumulative, "cumulative", torch.int64, E), _stream(stream))
+    _check(st, "moe_layout_accumulate_stats")
+
+
+def _host(t: torch.Tensor | None, name: str, allow_none=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous host tensor (page-locked for overlap)")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(s) -> ctypes.c_void_p:
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def dispatch_from_host(lay: "Layout", topk_idx_host, x_host, topk_idx, x, recv_x, weights_host=None, weights=None,
+                       sf_host=None, sf=None, recv_sf=None, chunk_tokens=0, stream=None, copy_stream=None) -> None:
+    """Host ids/rows in, layout + permuted rows on the device; copies overlapped with the permute."""
+    d = lay.desc
+    N, K = int(d.num_tokens), int(d.topk)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    if copy_stream is None:
+        raise ValueError("copy_stream is required (a stream other than `stream`)")
+    rb = x_host.shape[1] * x_host.element_size()
+    srb = sf_host.shape[1] * sf_host.element_size() if sf_host is not None else 0
+    st = load_library().moe_dispatch_from_host(
+        ctypes.byref(_desc(d)), _host(topk_idx_host, "topk_idx_host"), _host(x_host, "x_host"), rb,
+        _host(sf_host, "sf_host", True), srb, _host(weights_host, "weights_host", True),
+        _dev(topk_idx, "topk_idx", torch.int64, N * K), _dev(x, "x"), _dev(sf, "sf", allow_none=True),
+        _dev(weights, "weights", torch.float32, N * K, allow_none=True),
+        _dev(lay.expert_count, "expert_count"), _dev(lay.rank_count, "rank_count"),
+        _dev(lay.expert_offset, "expert_offset"), _dev(lay.rank_psum, "rank_psum"), _dev(lay.dst_slot, "dst_slot"),
+        _dev(lay.src_idx, "src_idx"), _dev(lay.total_rows, "total_rows"), _dev(recv_x, "recv_x"),
+        _dev(recv_sf, "recv_sf", allow_none=True), recv_x.shape[0], _dev(lay.workspace, "workspace"),
+        lay.workspace.numel(), int(chunk_tokens), _stream_ptr(s), _stream_ptr(copy_stream))
+    _check(st, "moe_dispatch_from_host")
+
+
+def combine_to_host(lay: "Layout", expert_out, weights, out, out_host, chunk_tokens=0, stream=None,
+                    copy_stream=None) -> None:
+    """Combine on the device with each chunk's result copied to ``out_host`` while the next is combined."""
+    d = lay.desc
+    N, K = int(d.num_tokens), int(d.topk)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    if copy_stream is None:
+        raise ValueError("copy_stream is required (a stream other than `stream`)")
+    if expert_out.dtype != torch.bfloat16 or out.dtype != torch.bfloat16 or out_host.dtype != torch.bfloat16:
+        raise ValueError("expert_out, out and out_host must be bfloat16")
+    st = load_library().moe_combine_to_host(
+        ctypes.byref(_desc(d)), _dev(expert_out, "expert_out"), expert_out.shape[0], expert_out.shape[1],
+        _dev(lay.dst_slot, "dst_slot", torch.int32, N * K), _dev(weights, "weights", torch.float32, N * K),
+        _dev(out, "out"), _host(out_host, "out_host"), _dev(lay.workspace, "workspace"), lay.workspace.numel(),
+        int(chunk_tokens), _stream_ptr(s), _stream_ptr(copy_stream))
+    _check(st, "moe_combine_to_host")
 
 
 def get_error(workspace, stream=None) -> int:

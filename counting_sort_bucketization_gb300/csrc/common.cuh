@@ -17,7 +17,10 @@ constexpr int kWarpSize = 32;
 constexpr int kLayoutWarps = 8;                        // warps per count / rank CTA
 constexpr int kLayoutThreads = kLayoutWarps * kWarpSize;
 constexpr int kMaxChunksPerWarp = 16;
-constexpr int kTargetTiles = 256;                      // tiles the plan aims for
+#ifndef MOE_LAYOUT_TARGET_TILES
+#define MOE_LAYOUT_TARGET_TILES 256
+#endif
+constexpr int kTargetTiles = MOE_LAYOUT_TARGET_TILES;   // tiles the plan aims for
 constexpr uint64_t kWaitLimitNs = 1000000000ull;       // 1 s bound on any in-kernel wait
 
 // The count and rank kernels walk topk_idx in token-aligned chunks of one warp:

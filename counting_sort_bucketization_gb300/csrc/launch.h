@@ -32,6 +32,9 @@ cudaError_t launch_build(const moe_layout_desc& d, const TilePlan& p, const int6
                          int32_t* src_idx, int64_t capacity, int32_t* total_rows, int* err,
                          cudaStream_t stream);
 
+// cumulative[e] += expert_count[e] (int64 running totals across calls).
+cudaError_t launch_accumulate_stats(const int32_t* expert_count, int E, int64_t* cumulative, cudaStream_t stream);
+
 // rank_rows_kernel: the non-expand (rank-contiguous) slot map.
 cudaError_t launch_rank_rows(const moe_layout_desc& d, const TilePlan& p, const int64_t* topk_idx,
                              const int32_t* rhist_prefix, const int32_t* rank_count, int32_t* rank_slot,

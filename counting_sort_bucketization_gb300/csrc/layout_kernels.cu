@@ -538,6 +538,16 @@ __global__ void __launch_bounds__(kLayoutThreads)
   }
 }
 
+// Running per-expert totals across calls ([CS] §7.2: the receive statistics
+// the page accumulates next to the alignment): cumulative[e] += count[e].
+__global__ void __launch_bounds__(kLayoutThreads)
+    accumulate_stats_kernel(const int32_t* __restrict__ expert_count, int E, int64_t* __restrict__ cumulative) {
+  ptx::grid_dependency_wait();
+  ptx::grid_dependency_launch_dependents();
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += gridDim.x * blockDim.x)
+    cumulative[e] += __ldcg(expert_count + e);
+}
+
 size_t fused_smem_bytes(const moe_layout_desc& d, const TilePlan& p) {
   const size_t pairs = static_cast<size_t>(p.tile_tokens) * d.topk;
   const size_t E = d.num_experts;
@@ -631,6 +641,14 @@ cudaError_t launch_rank(const moe_layout_desc& d, const TilePlan& p, const int64
                                src_idx, capacity, total_rows, err);
   st = launch_pdl(rank_maps_kernel, dim3(static_cast<unsigned>(grid)), dim3(kLayoutThreads), smem, stream,
                   topk_idx, p, a);
+  if (st != cudaSuccess) return st;
+  count_launch();
+  return cudaSuccess;
+}
+
+cudaError_t launch_accumulate_stats(const int32_t* expert_count, int E, int64_t* cumulative, cudaStream_t stream) {
+  const cudaError_t st = launch_pdl(accumulate_stats_kernel, dim3((E + kLayoutThreads - 1) / kLayoutThreads),
+                                    dim3(kLayoutThreads), 0, stream, expert_count, E, cumulative);
   if (st != cudaSuccess) return st;
   count_launch();
   return cudaSuccess;

@@ -243,6 +243,14 @@ int moe_combine_unpermute(const moe_layout_desc* desc, const void* expert_out, i
   return cuda_status(launch_combine(a, static_cast<cudaStream_t>(stream)));
 }
 
+int moe_layout_accumulate_stats(const moe_layout_desc* desc, const int32_t* expert_count, int64_t* cumulative,
+                                void* stream) {
+  if (int st = check_desc(desc)) return st;
+  if (expert_count == nullptr || cumulative == nullptr || !aligned(cumulative, 8)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_accumulate_stats(expert_count, desc->num_experts, cumulative,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
 int moe_layout_get_error(void* workspace, int32_t* device_error, void* stream) {
   if (workspace == nullptr || device_error == nullptr) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

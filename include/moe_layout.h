@@ -241,6 +241,56 @@ MOE_API int moe_layout_build_noalloc(const moe_layout_desc* desc, const int64_t*
                                      int32_t* total_rows, int32_t* device_error, void* stream);
 
 /*
+ * Running receive statistics ([CS] §7.2 keeps per-expert totals across
+ * calls next to the alignment step): cumulative[e] += expert_count[e] for
+ * every e, on `stream`, after a layout call.  cumulative is a caller-owned
+ * device int64 [E] the caller zeroes once.
+ */
+MOE_API int moe_layout_accumulate_stats(const moe_layout_desc* desc, const int32_t* expert_count,
+                                        int64_t* cumulative, void* stream);
+
+/*
+ * Dispatch straight from host memory: the ids (and, if given, the top-k
+ * weights and fp8 scale factors) are copied to the caller's device staging
+ * buffers, the layout is built (moe_layout_build), and the token rows are
+ * copied in chunks of chunk_tokens tokens (0 = one chunk) on copy_stream
+ * while the permute (moe_dispatch_permute, zero padding on the first chunk)
+ * of each chunk runs on `stream` as soon as its rows have landed.  Results
+ * and errors are those of the two calls; on return everything is enqueued
+ * on `stream` (copy_stream is joined into it).  Host buffers must be
+ * page-locked for the copies to overlap.  A pipeline around the method's
+ * steps; the pages have no counterpart to it.
+ *   topk_idx_host [N*K] int64, x_host [N, row_bytes], sf_host [N, sf_row_bytes]
+ *   or NULL, weights_host [N*K] fp32 or NULL (with weights NULL too);
+ *   topk_idx, x, sf, weights: device buffers of the same sizes.
+ */
+MOE_API int moe_dispatch_from_host(const moe_layout_desc* desc, const int64_t* topk_idx_host,
+                                   const void* x_host, int64_t row_bytes, const void* sf_host,
+                                   int64_t sf_row_bytes, const float* weights_host,
+                                   int64_t* topk_idx, void* x, void* sf, float* weights,
+                                   int32_t* expert_count, int32_t* rank_count,
+                                   int32_t* expert_offset, int32_t* rank_psum,
+                                   int32_t* dst_slot, int32_t* src_idx, int32_t* total_rows,
+                                   void* recv_x, void* recv_sf, int64_t capacity_rows,
+                                   void* workspace, size_t workspace_bytes,
+                                   int64_t chunk_tokens, void* stream, void* copy_stream);
+
+/*
+ * Combine straight to host memory: moe_combine_unpermute runs in chunks of
+ * chunk_tokens tokens (0 = one chunk) on `stream` into the device buffer
+ * `out` [N, hidden] bf16, and each chunk is copied to out_host on
+ * copy_stream while the next chunk is combined; copy_stream is joined into
+ * `stream` at the end, so synchronising `stream` covers the copies.
+ * out_host must be page-locked for the copies to overlap.  A pipeline
+ * around the method's steps; the pages have no counterpart to it.
+ */
+MOE_API int moe_combine_to_host(const moe_layout_desc* desc, const void* expert_out,
+                                int64_t expert_out_rows, int64_t hidden,
+                                const int32_t* dst_slot, const float* weights, void* out,
+                                void* out_host, void* workspace, size_t workspace_bytes,
+                                int64_t chunk_tokens, void* stream, void* copy_stream);
+
+/*
  * Synchronise `stream`, copy the workspace's sticky error word (the first
  * device-side error since the last read; MOE_OK if none) into
  * *device_error, and reset it to MOE_OK.

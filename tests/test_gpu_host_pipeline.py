@@ -1,0 +1,82 @@
+"""Dispatch from host memory and combine to host memory, with the copies
+overlapped with the kernels in chunks: results must equal the oracle's for
+any chunk size (one chunk, ragged chunks, one token per chunk)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from counting_sort_bucketization_gb300 import binding, build, workloads as wl
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+    binding.load_library()
+
+
+def u8(t):
+    t = t.detach().contiguous().cpu()
+    return t.view(torch.uint8).numpy().reshape(t.shape[0], -1) if t.numel() else np.zeros((t.shape[0], 0), np.uint8)
+
+
+def pipeline_case(w, seed, chunk):
+    inp = wl.make(w, seed)
+    N, K, H = w.num_tokens, w.topk, w.hidden
+    cap = wl.worst_case_rows(w)
+    idx_h = inp["topk_idx"].pin_memory()
+    x_h = inp["x"].pin_memory()
+    wt_h = inp["weights"].pin_memory()
+    sf_h = inp["sf"].pin_memory() if inp["sf"] is not None else None
+    idx_d = torch.empty_like(inp["topk_idx"], device=DEV)
+    x_d = torch.empty_like(inp["x"], device=DEV)
+    wt_d = torch.empty_like(inp["weights"], device=DEV)
+    sf_d = torch.empty_like(inp["sf"], device=DEV) if sf_h is not None else None
+    recv = torch.zeros((cap, H), dtype=torch.uint8, device=DEV).view(x_d.dtype) if x_d.element_size() == 1 \
+        else torch.full((cap, H), -7.0, dtype=x_d.dtype, device=DEV)
+    recv_sf = torch.full((cap, sf_d.shape[1]), -3.0, device=DEV) if sf_d is not None else None
+    lay = binding.Layout(w, cap, device=DEV)
+    copy = torch.cuda.Stream()
+    binding.dispatch_from_host(lay, idx_h, x_h, idx_d, x_d, recv, weights_host=wt_h, weights=wt_d, sf_host=sf_h,
+                               sf=sf_d, recv_sf=recv_sf, chunk_tokens=chunk, copy_stream=copy)
+    torch.cuda.synchronize()
+    assert lay.error() == 0
+    ref = oracle.layout(inp["topk_idx"].numpy(), w.num_experts, w.num_ranks, w.alignment, capacity_rows=cap)
+    rows = ref["total_rows"]
+    np.testing.assert_array_equal(lay.dst_slot[: N * K].cpu().numpy().reshape(N, K), ref["dst_slot"])
+    _, ref_recv, ref_sf = oracle.permute(u8(inp["x"]), ref["dst_slot"], ref["expert_offset"], ref["expert_count"],
+                                         rows, sf_bytes=u8(inp["sf"]) if sf_h is not None else None)
+    np.testing.assert_array_equal(u8(recv[:rows]), ref_recv)
+    if sf_h is not None:
+        np.testing.assert_array_equal(u8(recv_sf[:rows]), ref_sf)
+        return
+    np.testing.assert_array_equal(wt_d.cpu().numpy(), inp["weights"].numpy())
+    eo = recv[:rows].contiguous()
+    out = torch.empty((N, H), dtype=torch.bfloat16, device=DEV)
+    out_h = torch.full((N, H), 3.0, dtype=torch.bfloat16).pin_memory()
+    binding.combine_to_host(lay, eo, wt_d, out, out_h, chunk_tokens=chunk, copy_stream=copy)
+    torch.cuda.current_stream().synchronize()
+    assert lay.error() == 0
+    ref_out = oracle.combine(ref_recv.view(np.uint16).reshape(rows, H), ref["dst_slot"], inp["weights"].numpy())
+    np.testing.assert_array_equal(out_h.view(torch.int16).numpy().view(np.uint16), ref_out)
+
+
+@pytest.mark.parametrize("chunk", [0, 100, 1])
+def test_tiny(chunk):
+    pipeline_case(wl.WORKLOADS["tiny"], 0, chunk)
+
+
+@pytest.mark.parametrize("chunk", [0, 1000])
+def test_decode(chunk):
+    pipeline_case(wl.WORKLOADS["decode"], 1, chunk)
+
+
+def test_fp8_rows_with_scale_factors():
+    pipeline_case(wl.WORKLOADS["prefill_fp8"].replace(num_tokens=3000), 3, 512)
+
+
+def test_masked_and_ragged():
+    pipeline_case(wl.Workload("edge", 777, 4, 24, 6, 8, 64, mask_prob=0.3), 7, 100)

@@ -324,3 +324,35 @@ def test_kernel_launch_counter_moves():
     before = binding.kernel_launches()
     full_case(wl.WORKLOADS["tiny"], 0, fused=True)
     assert binding.kernel_launches() - before == 3     # fused layout, permute, combine
+
+
+def test_cached_dispatch_reuses_the_layout():
+    """Cached mode (the page keeps the slot map and skips counting on a second
+    dispatch): the same dst_slot moves a second tensor with other row bytes."""
+    w = wl.WORKLOADS["skewed"].replace(num_tokens=3000, hidden=64)
+    inp = wl.make(w, 12)
+    cap = wl.worst_case_rows(w)
+    lay = run_gpu_layout(w, inp["topk_idx"], cap)
+    ref = oracle.layout(inp["topk_idx"].numpy(), w.num_experts, w.num_ranks, w.alignment, capacity_rows=cap)
+    rows = ref["total_rows"]
+    launches = binding.kernel_launches()
+    for cols, dtype in ((64, torch.bfloat16), (96, torch.float32), (16, torch.uint8)):
+        y = (torch.arange(3000 * cols, dtype=torch.float32).reshape(3000, cols) % 251).to(dtype)
+        recv = torch.full((cap, cols), 7, dtype=dtype, device=DEV)
+        lay.permute(y.to(DEV), recv)
+        _, want, _ = oracle.permute(u8(y), ref["dst_slot"], ref["expert_offset"], ref["expert_count"], rows)
+        np.testing.assert_array_equal(u8(recv[:rows]), want)
+    assert binding.kernel_launches() - launches == 3     # permutes only, no recount
+    assert lay.error() == 0
+
+
+def test_cumulative_expert_stats():
+    w = wl.WORKLOADS["decode"]
+    cum = torch.zeros(w.num_experts, dtype=torch.int64, device=DEV)
+    want = np.zeros(w.num_experts, np.int64)
+    for seed in (1, 2, 3):
+        idx = wl.draw_topk_idx(w, seed)
+        lay = run_gpu_layout(w, idx, wl.worst_case_rows(w))
+        binding.accumulate_stats(w, lay.expert_count, cum)
+        want += oracle.layout(idx.numpy(), w.num_experts, w.num_ranks, w.alignment)["expert_count"]
+    np.testing.assert_array_equal(cum.cpu().numpy(), want)
