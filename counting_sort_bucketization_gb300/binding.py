@@ -73,6 +73,7 @@ def load_library() -> ctypes.CDLL:
         lib.moe_layout_count.argtypes = [dp, p, p, p, p, sz, p]
         lib.moe_layout_scan.argtypes = [dp, p, p, p, p, sz, p, p, p, p, i64, p, p]
         lib.moe_layout_build.argtypes = [dp, p, p, p, p, sz, p, p, p, p, i64, p, p]
+        lib.moe_layout_build_i32.argtypes = [dp, p, p, p, p, sz, p, p, p, p, i64, p, p]
         lib.moe_dispatch_permute.argtypes = [dp, p, i64, p, i64, p, p, p, p, p, i64, ctypes.c_int, p, sz, p]
         lib.moe_layout_rank_rows.argtypes = [dp, p, p, p, sz, p, p, i64, p]
         lib.moe_layout_accumulate_stats.argtypes = [dp, p, p, p]
@@ -87,6 +88,7 @@ def load_library() -> ctypes.CDLL:
         lib.moe_kernel_launches.argtypes = []
         lib.moe_kernel_launches.restype = ctypes.c_uint64
         for name in ("moe_layout_workspace_bytes", "moe_layout_count", "moe_layout_scan", "moe_layout_build",
+                     "moe_layout_build_i32",
                      "moe_layout_rank_rows", "moe_dispatch_permute_ranks", "moe_dispatch_from_host",
                      "moe_combine_to_host", "moe_layout_accumulate_stats",
                      "moe_dispatch_permute", "moe_combine_unpermute", "moe_layout_get_error"):
@@ -170,10 +172,14 @@ def layout_scan(desc, topk_idx, expert_count, rank_count, workspace, expert_offs
 
 def layout_build(desc, topk_idx, expert_count, rank_count, workspace, expert_offset, rank_psum, dst_slot,
                  src_idx, total_rows, stream=None) -> None:
-    """layout_count + layout_scan in one call (one cooperative kernel when it fits)."""
+    """layout_count + layout_scan in one call (one cooperative kernel when it fits).
+    ``topk_idx`` may be int64 or int32."""
     N, K, E, R = int(desc.num_tokens), int(desc.topk), int(desc.num_experts), int(desc.num_ranks)
-    st = load_library().moe_layout_build(
-        ctypes.byref(_desc(desc)), _dev(topk_idx, "topk_idx", torch.int64, N * K),
+    lib = load_library()
+    fn = lib.moe_layout_build_i32 if topk_idx.dtype == torch.int32 else lib.moe_layout_build
+    st = fn(
+        ctypes.byref(_desc(desc)), _dev(topk_idx, "topk_idx", topk_idx.dtype if topk_idx.dtype == torch.int32
+                                        else torch.int64, N * K),
         _dev(expert_count, "expert_count", torch.int32, E), _dev(rank_count, "rank_count", torch.int32, R),
         _dev(workspace, "workspace", torch.uint8), workspace.numel(),
         _dev(expert_offset, "expert_offset", torch.int32, E + 1), _dev(rank_psum, "rank_psum", torch.int32, R),

@@ -60,14 +60,30 @@ __global__ void __launch_bounds__(kCombineThreads)
   const int ntok = static_cast<int>(max64(0, min64(tokens_per_cta, a.num_tokens - t0)));
   ptx::grid_dependency_wait();
   ptx::grid_dependency_launch_dependents();
-  for (int i = threadIdx.x; i < ntok * K; i += kCombineThreads) {
-    int s = __ldg(a.dst_slot + t0 * K + i);
-    if (s >= a.expert_out_rows) {
-      set_error(a.err, MOE_ERR_CAPACITY);
-      s = -1;
+  // Slots and weights of the CTA's tokens; kBatch independent loads of each per thread.
+  constexpr int kBatch = 4;
+  for (int base = threadIdx.x; base < ntok * K; base += kBatch * kCombineThreads) {
+    int sv[kBatch];
+    float wv[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = base + u * kCombineThreads;
+      const bool in = i < ntok * K;
+      sv[u] = in ? __ldg(a.dst_slot + t0 * K + i) : -1;
+      wv[u] = in ? __ldg(a.weights + t0 * K + i) : 0.0f;
     }
-    slot_s[i] = s;
-    w_s[i] = __ldg(a.weights + t0 * K + i);
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = base + u * kCombineThreads;
+      if (i >= ntok * K) break;
+      int s = sv[u];
+      if (s >= a.expert_out_rows) {
+        set_error(a.err, MOE_ERR_CAPACITY);
+        s = -1;
+      }
+      slot_s[i] = s;
+      w_s[i] = wv[u];
+    }
   }
   __syncthreads();
 

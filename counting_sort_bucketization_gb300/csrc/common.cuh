@@ -9,7 +9,7 @@
 #include <cstdint>
 #include <utility>
 
-#include "../../include/moe_layout.h"
+#include "moe_layout.h"  // include/ is on the include path
 
 namespace moe {
 
@@ -60,6 +60,7 @@ inline TilePlan make_tile_plan(int64_t N, int K) {
 struct WorkspaceLayout {
   size_t err_off = 0;
   size_t bar_off = 16;   // two unsigned: arrival counter, generation
+  size_t work_off = 32;  // two unsigned: permute's token counter, finished CTAs
   size_t hist_off = 256;
   size_t rhist_off = 0;
   size_t bytes = 0;

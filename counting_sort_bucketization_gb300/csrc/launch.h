@@ -12,33 +12,36 @@ namespace moe {
 size_t count_smem_bytes(const moe_layout_desc& d, const TilePlan& p);
 size_t rank_smem_bytes(const moe_layout_desc& d, const TilePlan& p);
 
+// topk_idx as int64 (the default) or int32.
+struct IdsRef {
+  const void* ptr;
+  bool i32;
+};
+
 // count_tiles_kernel + scan_columns_kernel.
-cudaError_t launch_count(const moe_layout_desc& d, const TilePlan& p, const int64_t* topk_idx,
-                         int32_t* expert_count, int32_t* rank_count, int* err, int32_t* hist,
-                         int32_t* rhist, cudaStream_t stream);
+cudaError_t launch_count(const moe_layout_desc& d, const TilePlan& p, IdsRef ids, int32_t* expert_count,
+                         int32_t* rank_count, int* err, int32_t* hist, int32_t* rhist, cudaStream_t stream);
 
 // rank_maps_kernel.
-cudaError_t launch_rank(const moe_layout_desc& d, const TilePlan& p, const int64_t* topk_idx,
-                        const int32_t* hist_prefix, const int32_t* expert_count,
-                        const int32_t* rank_count, int32_t* expert_offset, int32_t* rank_psum,
-                        int32_t* dst_slot, int32_t* src_idx, int64_t capacity,
+cudaError_t launch_rank(const moe_layout_desc& d, const TilePlan& p, IdsRef ids, const int32_t* hist_prefix,
+                        const int32_t* expert_count, const int32_t* rank_count, int32_t* expert_offset,
+                        int32_t* rank_psum, int32_t* dst_slot, int32_t* src_idx, int64_t capacity,
                         int32_t* total_rows, int* err, cudaStream_t stream);
 
 // Count + scan + rank: one cooperative kernel when every tile fits on the
 // GPU at once, else the three kernels above.
-cudaError_t launch_build(const moe_layout_desc& d, const TilePlan& p, const int64_t* topk_idx,
-                         int32_t* expert_count, int32_t* rank_count, int32_t* hist, int32_t* rhist,
-                         unsigned* barrier_words, int32_t* expert_offset, int32_t* rank_psum, int32_t* dst_slot,
-                         int32_t* src_idx, int64_t capacity, int32_t* total_rows, int* err,
-                         cudaStream_t stream);
+cudaError_t launch_build(const moe_layout_desc& d, const TilePlan& p, IdsRef ids, int32_t* expert_count,
+                         int32_t* rank_count, int32_t* hist, int32_t* rhist, unsigned* barrier_words,
+                         int32_t* expert_offset, int32_t* rank_psum, int32_t* dst_slot, int32_t* src_idx,
+                         int64_t capacity, int32_t* total_rows, int* err, cudaStream_t stream);
 
 // cumulative[e] += expert_count[e] (int64 running totals across calls).
 cudaError_t launch_accumulate_stats(const int32_t* expert_count, int E, int64_t* cumulative, cudaStream_t stream);
 
 // rank_rows_kernel: the non-expand (rank-contiguous) slot map.
-cudaError_t launch_rank_rows(const moe_layout_desc& d, const TilePlan& p, const int64_t* topk_idx,
-                             const int32_t* rhist_prefix, const int32_t* rank_count, int32_t* rank_slot,
-                             int32_t* rank_src, int64_t capacity, int* err, cudaStream_t stream);
+cudaError_t launch_rank_rows(const moe_layout_desc& d, const TilePlan& p, IdsRef ids, const int32_t* rhist_prefix,
+                             const int32_t* rank_count, int32_t* rank_slot, int32_t* rank_src, int64_t capacity,
+                             int* err, cudaStream_t stream);
 
 struct PermuteArgs {
   const uint8_t* x;
@@ -57,6 +60,7 @@ struct PermuteArgs {
   int num_experts;
   int zero_pad;
   int* err;
+  unsigned* work;                // [2] token counter + finished-CTA counter (zero between launches)
 };
 
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t stream);

@@ -39,20 +39,35 @@ constexpr unsigned kFull = 0xffffffffu;
 
 // Stage the tile's topk ids into shared memory as int32: masked -> -1,
 // id >= E -> -1 and flagged.
-__device__ __forceinline__ void stage_tile_ids(const int64_t* __restrict__ topk_idx,
+// Each thread issues kStageBatch independent loads before it uses any, so a
+// tile of thousands of pairs costs a few memory latencies, not one per pair.
+constexpr int kStageBatch = 8;
+
+template <typename IdT>
+__device__ __forceinline__ void stage_tile_ids(const IdT* __restrict__ topk_idx,
                                                int64_t pair0, int npairs, int E, int* ids_s,
                                                int* err) {
   bool bad = false;
-  for (int i = threadIdx.x; i < npairs; i += blockDim.x) {
-    const int64_t v = __ldg(topk_idx + pair0 + i);
-    int e = -1;
-    if (v >= 0) {
-      if (v < E)
-        e = static_cast<int>(v);
-      else
-        bad = true;
+  for (int base = threadIdx.x; base < npairs; base += kStageBatch * blockDim.x) {
+    int64_t v[kStageBatch];
+#pragma unroll
+    for (int u = 0; u < kStageBatch; ++u) {
+      const int i = base + u * blockDim.x;
+      v[u] = i < npairs ? __ldg(topk_idx + pair0 + i) : -1;
     }
-    ids_s[i] = e;
+#pragma unroll
+    for (int u = 0; u < kStageBatch; ++u) {
+      const int i = base + u * blockDim.x;
+      if (i >= npairs) break;
+      int e = -1;
+      if (v[u] >= 0) {
+        if (v[u] < E)
+          e = static_cast<int>(v[u]);
+        else
+          bad = true;
+      }
+      ids_s[i] = e;
+    }
   }
   if (bad) set_error(err, MOE_ERR_BAD_EXPERT_ID);
 }
@@ -317,8 +332,9 @@ __device__ void rank_phase(const TilePlan& plan, const RankArgs& a, int tile, Ti
 }
 
 // ---------------------------------------------------------- kernels
+template <typename IdT>
 __global__ void __launch_bounds__(kLayoutThreads)
-    count_tiles_kernel(const int64_t* __restrict__ topk_idx, int64_t N, int K, int E, int R,
+    count_tiles_kernel(const IdT* __restrict__ topk_idx, int64_t N, int K, int E, int R,
                        TilePlan plan, int32_t* __restrict__ hist, int32_t* __restrict__ rhist,
                        int* err) {
   extern __shared__ int smem[];
@@ -343,8 +359,9 @@ __global__ void __launch_bounds__(kLayoutThreads)
   scan_phase(hist, rhist, T, E, R, expert_count, rank_count);
 }
 
+template <typename IdT>
 __global__ void __launch_bounds__(kLayoutThreads)
-    rank_maps_kernel(const int64_t* __restrict__ topk_idx, TilePlan plan, RankArgs a) {
+    rank_maps_kernel(const IdT* __restrict__ topk_idx, TilePlan plan, RankArgs a) {
   extern __shared__ int smem[];
   int* off_s = smem;                            // [E+1]
   int* cnt_s = off_s + (a.E + 1);               // [kLayoutWarps][E]
@@ -390,8 +407,9 @@ __device__ bool grid_barrier(unsigned* arrive, unsigned* gen, unsigned nctas, in
   return *flag_s != 0;
 }
 
+template <typename IdT>
 __global__ void __launch_bounds__(kLayoutThreads)
-    layout_fused_kernel(const int64_t* __restrict__ topk_idx, TilePlan plan, RankArgs a, int32_t* hist,
+    layout_fused_kernel(const IdT* __restrict__ topk_idx, TilePlan plan, RankArgs a, int32_t* hist,
                         int32_t* rhist, int32_t* expert_count, int32_t* rank_count, unsigned* bar) {
   extern __shared__ int smem[];
   const int E = a.E, R = a.R, K = a.K;
@@ -438,8 +456,9 @@ struct RankRowsArgs {
   int* err;
 };
 
+template <typename IdT>
 __global__ void __launch_bounds__(kLayoutThreads)
-    rank_rows_kernel(const int64_t* __restrict__ topk_idx, TilePlan plan, RankRowsArgs a) {
+    rank_rows_kernel(const IdT* __restrict__ topk_idx, TilePlan plan, RankRowsArgs a) {
   extern __shared__ int smem[];
   const int K = a.K, E = a.E, R = a.R, L = E / R;
   int* start_s = smem;                          // [R+1] block starts, then the total
@@ -555,15 +574,16 @@ size_t fused_smem_bytes(const moe_layout_desc& d, const TilePlan& p) {
 }
 
 // Whether every tile's CTA of the fused kernel can be resident at once.
+template <typename IdT>
 bool fused_fits(const TilePlan& p, size_t smem) {
   int dev = 0, coop = 0, per_sm = 0;
   if (p.tiles < 1) return false;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop) return false;
-  if (cudaFuncSetAttribute(layout_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(layout_fused_kernel<IdT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return false;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layout_fused_kernel, kLayoutThreads, smem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layout_fused_kernel<IdT>, kLayoutThreads, smem) !=
       cudaSuccess)
     return false;
   return p.tiles <= static_cast<int64_t>(per_sm) * device_sm_count();
@@ -604,16 +624,17 @@ size_t rank_smem_bytes(const moe_layout_desc& d, const TilePlan& p) {
                         2 * static_cast<size_t>(p.tile_tokens) * d.topk);
 }
 
-cudaError_t launch_count(const moe_layout_desc& d, const TilePlan& p, const int64_t* topk_idx,
-                         int32_t* expert_count, int32_t* rank_count, int* err, int32_t* hist,
-                         int32_t* rhist, cudaStream_t stream) {
+namespace {
+
+template <typename IdT>
+cudaError_t launch_count_t(const moe_layout_desc& d, const TilePlan& p, const IdT* topk_idx, int32_t* expert_count,
+                           int32_t* rank_count, int* err, int32_t* hist, int32_t* rhist, cudaStream_t stream) {
   const size_t smem1 = count_smem_bytes(d, p);
-  cudaError_t st = cudaFuncSetAttribute(count_tiles_kernel,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t st = cudaFuncSetAttribute(count_tiles_kernel<IdT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(smem1));
   if (st != cudaSuccess) return st;
   if (p.tiles > 0) {
-    st = launch_pdl(count_tiles_kernel, dim3(static_cast<unsigned>(p.tiles)), dim3(kLayoutThreads), smem1,
+    st = launch_pdl(count_tiles_kernel<IdT>, dim3(static_cast<unsigned>(p.tiles)), dim3(kLayoutThreads), smem1,
                     stream, topk_idx, d.num_tokens, d.topk, d.num_experts, d.num_ranks, p, hist, rhist, err);
     if (st != cudaSuccess) return st;
     count_launch();
@@ -626,24 +647,83 @@ cudaError_t launch_count(const moe_layout_desc& d, const TilePlan& p, const int6
   return cudaSuccess;
 }
 
-cudaError_t launch_rank(const moe_layout_desc& d, const TilePlan& p, const int64_t* topk_idx,
-                        const int32_t* hist_prefix, const int32_t* expert_count,
-                        const int32_t* rank_count, int32_t* expert_offset, int32_t* rank_psum,
-                        int32_t* dst_slot, int32_t* src_idx, int64_t capacity,
-                        int32_t* total_rows, int* err, cudaStream_t stream) {
+template <typename IdT>
+cudaError_t launch_rank_t(const moe_layout_desc& d, const TilePlan& p, const IdT* topk_idx, const RankArgs& a,
+                          cudaStream_t stream) {
   const size_t smem = rank_smem_bytes(d, p);
-  cudaError_t st = cudaFuncSetAttribute(rank_maps_kernel,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t st = cudaFuncSetAttribute(rank_maps_kernel<IdT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(smem));
   if (st != cudaSuccess) return st;
   const int64_t grid = p.tiles > 0 ? p.tiles : 1;
-  const RankArgs a = rank_args(d, hist_prefix, expert_count, rank_count, expert_offset, rank_psum, dst_slot,
-                               src_idx, capacity, total_rows, err);
-  st = launch_pdl(rank_maps_kernel, dim3(static_cast<unsigned>(grid)), dim3(kLayoutThreads), smem, stream,
+  st = launch_pdl(rank_maps_kernel<IdT>, dim3(static_cast<unsigned>(grid)), dim3(kLayoutThreads), smem, stream,
                   topk_idx, p, a);
   if (st != cudaSuccess) return st;
   count_launch();
   return cudaSuccess;
+}
+
+template <typename IdT>
+cudaError_t launch_rank_rows_t(const moe_layout_desc& d, const TilePlan& p, const IdT* topk_idx,
+                               const RankRowsArgs& a, cudaStream_t stream) {
+  const size_t smem = sizeof(int) * (static_cast<size_t>(d.num_ranks) + 1 +
+                                     static_cast<size_t>(kLayoutWarps) * d.num_ranks +
+                                     2 * static_cast<size_t>(p.tile_tokens) * d.topk);
+  cudaError_t st = cudaFuncSetAttribute(rank_rows_kernel<IdT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(smem));
+  if (st != cudaSuccess) return st;
+  const int64_t grid = p.tiles > 0 ? p.tiles : 1;
+  st = launch_pdl(rank_rows_kernel<IdT>, dim3(static_cast<unsigned>(grid)), dim3(kLayoutThreads), smem, stream,
+                  topk_idx, p, a);
+  if (st != cudaSuccess) return st;
+  count_launch();
+  return cudaSuccess;
+}
+
+template <typename IdT>
+cudaError_t launch_build_t(const moe_layout_desc& d, const TilePlan& p, const IdT* topk_idx, int32_t* expert_count,
+                           int32_t* rank_count, int32_t* hist, int32_t* rhist, unsigned* barrier_words,
+                           const RankArgs& a, cudaStream_t stream) {
+  const size_t smem = fused_smem_bytes(d, p);
+  if (!fused_fits<IdT>(p, smem)) {
+    cudaError_t st = launch_count_t(d, p, topk_idx, expert_count, rank_count, a.err, hist, rhist, stream);
+    if (st != cudaSuccess) return st;
+    return launch_rank_t(d, p, topk_idx, a, stream);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.tiles));
+  cfg.blockDim = dim3(kLayoutThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t st = cudaLaunchKernelEx(&cfg, layout_fused_kernel<IdT>, topk_idx, p, a, hist, rhist,
+                                            expert_count, rank_count, barrier_words);
+  if (st != cudaSuccess) return st;
+  count_launch();
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_count(const moe_layout_desc& d, const TilePlan& p, IdsRef ids, int32_t* expert_count,
+                         int32_t* rank_count, int* err, int32_t* hist, int32_t* rhist, cudaStream_t stream) {
+  return ids.i32 ? launch_count_t(d, p, static_cast<const int32_t*>(ids.ptr), expert_count, rank_count, err, hist,
+                                  rhist, stream)
+                 : launch_count_t(d, p, static_cast<const int64_t*>(ids.ptr), expert_count, rank_count, err, hist,
+                                  rhist, stream);
+}
+
+cudaError_t launch_rank(const moe_layout_desc& d, const TilePlan& p, IdsRef ids, const int32_t* hist_prefix,
+                        const int32_t* expert_count, const int32_t* rank_count, int32_t* expert_offset,
+                        int32_t* rank_psum, int32_t* dst_slot, int32_t* src_idx, int64_t capacity,
+                        int32_t* total_rows, int* err, cudaStream_t stream) {
+  const RankArgs a = rank_args(d, hist_prefix, expert_count, rank_count, expert_offset, rank_psum, dst_slot,
+                               src_idx, capacity, total_rows, err);
+  return ids.i32 ? launch_rank_t(d, p, static_cast<const int32_t*>(ids.ptr), a, stream)
+                 : launch_rank_t(d, p, static_cast<const int64_t*>(ids.ptr), a, stream);
 }
 
 cudaError_t launch_accumulate_stats(const int32_t* expert_count, int E, int64_t* cumulative, cudaStream_t stream) {
@@ -654,15 +734,9 @@ cudaError_t launch_accumulate_stats(const int32_t* expert_count, int E, int64_t*
   return cudaSuccess;
 }
 
-cudaError_t launch_rank_rows(const moe_layout_desc& d, const TilePlan& p, const int64_t* topk_idx,
-                             const int32_t* rhist_prefix, const int32_t* rank_count, int32_t* rank_slot,
-                             int32_t* rank_src, int64_t capacity, int* err, cudaStream_t stream) {
-  const size_t smem = sizeof(int) * (static_cast<size_t>(d.num_ranks) + 1 +
-                                     static_cast<size_t>(kLayoutWarps) * d.num_ranks +
-                                     2 * static_cast<size_t>(p.tile_tokens) * d.topk);
-  cudaError_t st = cudaFuncSetAttribute(rank_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(smem));
-  if (st != cudaSuccess) return st;
+cudaError_t launch_rank_rows(const moe_layout_desc& d, const TilePlan& p, IdsRef ids, const int32_t* rhist_prefix,
+                             const int32_t* rank_count, int32_t* rank_slot, int32_t* rank_src, int64_t capacity,
+                             int* err, cudaStream_t stream) {
   RankRowsArgs a;
   a.N = d.num_tokens;
   a.K = d.topk;
@@ -674,43 +748,20 @@ cudaError_t launch_rank_rows(const moe_layout_desc& d, const TilePlan& p, const 
   a.rank_src = rank_src;
   a.capacity = capacity;
   a.err = err;
-  const int64_t grid = p.tiles > 0 ? p.tiles : 1;
-  st = launch_pdl(rank_rows_kernel, dim3(static_cast<unsigned>(grid)), dim3(kLayoutThreads), smem, stream,
-                  topk_idx, p, a);
-  if (st != cudaSuccess) return st;
-  count_launch();
-  return cudaSuccess;
+  return ids.i32 ? launch_rank_rows_t(d, p, static_cast<const int32_t*>(ids.ptr), a, stream)
+                 : launch_rank_rows_t(d, p, static_cast<const int64_t*>(ids.ptr), a, stream);
 }
 
-cudaError_t launch_build(const moe_layout_desc& d, const TilePlan& p, const int64_t* topk_idx,
-                         int32_t* expert_count, int32_t* rank_count, int32_t* hist, int32_t* rhist,
-                         unsigned* barrier_words, int32_t* expert_offset, int32_t* rank_psum, int32_t* dst_slot,
-                         int32_t* src_idx, int64_t capacity, int32_t* total_rows, int* err,
-                         cudaStream_t stream) {
-  const size_t smem = fused_smem_bytes(d, p);
-  if (!fused_fits(p, smem)) {
-    cudaError_t st = launch_count(d, p, topk_idx, expert_count, rank_count, err, hist, rhist, stream);
-    if (st != cudaSuccess) return st;
-    return launch_rank(d, p, topk_idx, hist, expert_count, rank_count, expert_offset, rank_psum, dst_slot,
-                       src_idx, capacity, total_rows, err, stream);
-  }
+cudaError_t launch_build(const moe_layout_desc& d, const TilePlan& p, IdsRef ids, int32_t* expert_count,
+                         int32_t* rank_count, int32_t* hist, int32_t* rhist, unsigned* barrier_words,
+                         int32_t* expert_offset, int32_t* rank_psum, int32_t* dst_slot, int32_t* src_idx,
+                         int64_t capacity, int32_t* total_rows, int* err, cudaStream_t stream) {
   const RankArgs a = rank_args(d, hist, expert_count, rank_count, expert_offset, rank_psum, dst_slot, src_idx,
                                capacity, total_rows, err);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.tiles));
-  cfg.blockDim = dim3(kLayoutThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t st = cudaLaunchKernelEx(&cfg, layout_fused_kernel, topk_idx, p, a, hist, rhist,
-                                            expert_count, rank_count, barrier_words);
-  if (st != cudaSuccess) return st;
-  count_launch();
-  return cudaSuccess;
+  return ids.i32 ? launch_build_t(d, p, static_cast<const int32_t*>(ids.ptr), expert_count, rank_count, hist, rhist,
+                                  barrier_words, a, stream)
+                 : launch_build_t(d, p, static_cast<const int64_t*>(ids.ptr), expert_count, rank_count, hist, rhist,
+                                  barrier_words, a, stream);
 }
 
 }  // namespace moe

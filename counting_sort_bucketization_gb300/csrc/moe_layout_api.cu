@@ -85,7 +85,7 @@ int moe_layout_count(const moe_layout_desc* desc, const int64_t* topk_idx, int32
   if ((desc->num_tokens > 0 && topk_idx == nullptr) || expert_count == nullptr || rank_count == nullptr)
     return MOE_ERR_INVALID_ARG;
   const TilePlan p = make_tile_plan(desc->num_tokens, desc->topk);
-  return cuda_status(launch_count(*desc, p, topk_idx, expert_count, rank_count, at<int>(workspace, w.err_off),
+  return cuda_status(launch_count(*desc, p, IdsRef{topk_idx, false}, expert_count, rank_count, at<int>(workspace, w.err_off),
                                   at<int32_t>(workspace, w.hist_off), at<int32_t>(workspace, w.rhist_off),
                                   static_cast<cudaStream_t>(stream)));
 }
@@ -103,28 +103,44 @@ int moe_layout_scan(const moe_layout_desc* desc, const int64_t* topk_idx, const 
     return MOE_ERR_INVALID_ARG;
   if (capacity_rows < 0 || (capacity_rows > 0 && src_idx == nullptr)) return MOE_ERR_INVALID_ARG;
   const TilePlan p = make_tile_plan(desc->num_tokens, desc->topk);
-  return cuda_status(launch_rank(*desc, p, topk_idx, at<int32_t>(workspace, w.hist_off), expert_count,
+  return cuda_status(launch_rank(*desc, p, IdsRef{topk_idx, false}, at<int32_t>(workspace, w.hist_off), expert_count,
                                  rank_count, expert_offset, rank_psum, dst_slot, src_idx, capacity_rows,
                                  total_rows, at<int>(workspace, w.err_off), static_cast<cudaStream_t>(stream)));
+}
+
+static int build_impl(const moe_layout_desc* desc, IdsRef ids, int32_t* expert_count, int32_t* rank_count,
+                      void* workspace, size_t workspace_bytes, int32_t* expert_offset, int32_t* rank_psum,
+                      int32_t* dst_slot, int32_t* src_idx, int64_t capacity_rows, int32_t* total_rows,
+                      void* stream) {
+  if (int st = check_desc(desc)) return st;
+  WorkspaceLayout w;
+  if (int st = check_workspace(desc, workspace, workspace_bytes, &w)) return st;
+  const bool has_pairs = desc->num_tokens > 0;
+  if ((has_pairs && (ids.ptr == nullptr || dst_slot == nullptr)) || expert_count == nullptr ||
+      rank_count == nullptr || expert_offset == nullptr || rank_psum == nullptr || total_rows == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (capacity_rows < 0 || (capacity_rows > 0 && src_idx == nullptr)) return MOE_ERR_INVALID_ARG;
+  const TilePlan p = make_tile_plan(desc->num_tokens, desc->topk);
+  return cuda_status(launch_build(*desc, p, ids, expert_count, rank_count, at<int32_t>(workspace, w.hist_off),
+                                  at<int32_t>(workspace, w.rhist_off), at<unsigned>(workspace, w.bar_off),
+                                  expert_offset, rank_psum, dst_slot, src_idx, capacity_rows, total_rows,
+                                  at<int>(workspace, w.err_off), static_cast<cudaStream_t>(stream)));
 }
 
 int moe_layout_build(const moe_layout_desc* desc, const int64_t* topk_idx, int32_t* expert_count,
                      int32_t* rank_count, void* workspace, size_t workspace_bytes, int32_t* expert_offset,
                      int32_t* rank_psum, int32_t* dst_slot, int32_t* src_idx, int64_t capacity_rows,
                      int32_t* total_rows, void* stream) {
-  if (int st = check_desc(desc)) return st;
-  WorkspaceLayout w;
-  if (int st = check_workspace(desc, workspace, workspace_bytes, &w)) return st;
-  const bool has_pairs = desc->num_tokens > 0;
-  if ((has_pairs && (topk_idx == nullptr || dst_slot == nullptr)) || expert_count == nullptr ||
-      rank_count == nullptr || expert_offset == nullptr || rank_psum == nullptr || total_rows == nullptr)
-    return MOE_ERR_INVALID_ARG;
-  if (capacity_rows < 0 || (capacity_rows > 0 && src_idx == nullptr)) return MOE_ERR_INVALID_ARG;
-  const TilePlan p = make_tile_plan(desc->num_tokens, desc->topk);
-  return cuda_status(launch_build(*desc, p, topk_idx, expert_count, rank_count, at<int32_t>(workspace, w.hist_off),
-                                  at<int32_t>(workspace, w.rhist_off), at<unsigned>(workspace, w.bar_off),
-                                  expert_offset, rank_psum, dst_slot, src_idx, capacity_rows, total_rows,
-                                  at<int>(workspace, w.err_off), static_cast<cudaStream_t>(stream)));
+  return build_impl(desc, IdsRef{topk_idx, false}, expert_count, rank_count, workspace, workspace_bytes,
+                    expert_offset, rank_psum, dst_slot, src_idx, capacity_rows, total_rows, stream);
+}
+
+int moe_layout_build_i32(const moe_layout_desc* desc, const int32_t* topk_idx, int32_t* expert_count,
+                         int32_t* rank_count, void* workspace, size_t workspace_bytes, int32_t* expert_offset,
+                         int32_t* rank_psum, int32_t* dst_slot, int32_t* src_idx, int64_t capacity_rows,
+                         int32_t* total_rows, void* stream) {
+  return build_impl(desc, IdsRef{topk_idx, true}, expert_count, rank_count, workspace, workspace_bytes,
+                    expert_offset, rank_psum, dst_slot, src_idx, capacity_rows, total_rows, stream);
 }
 
 int moe_dispatch_permute(const moe_layout_desc* desc, const void* x, int64_t row_bytes, const void* sf,
@@ -162,6 +178,7 @@ int moe_dispatch_permute(const moe_layout_desc* desc, const void* x, int64_t row
   a.num_experts = desc->num_experts;
   a.zero_pad = zero_pad != 0;
   a.err = at<int>(workspace, w.err_off);
+  a.work = at<unsigned>(workspace, w.work_off);
   return cuda_status(launch_permute(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -175,7 +192,7 @@ int moe_layout_rank_rows(const moe_layout_desc* desc, const int64_t* topk_idx, c
   if ((has_pairs && (topk_idx == nullptr || rank_slot == nullptr)) || rank_count == nullptr) return MOE_ERR_INVALID_ARG;
   if (capacity_rows < 0 || (capacity_rows > 0 && rank_src == nullptr)) return MOE_ERR_INVALID_ARG;
   const TilePlan p = make_tile_plan(desc->num_tokens, desc->topk);
-  return cuda_status(launch_rank_rows(*desc, p, topk_idx, at<int32_t>(workspace, w.rhist_off), rank_count, rank_slot,
+  return cuda_status(launch_rank_rows(*desc, p, IdsRef{topk_idx, false}, at<int32_t>(workspace, w.rhist_off), rank_count, rank_slot,
                                       rank_src, capacity_rows, at<int>(workspace, w.err_off),
                                       static_cast<cudaStream_t>(stream)));
 }
@@ -215,6 +232,7 @@ int moe_dispatch_permute_ranks(const moe_layout_desc* desc, const void* x, int64
   a.num_experts = desc->num_experts;
   a.zero_pad = 0;
   a.err = at<int>(workspace, w.err_off);
+  a.work = at<unsigned>(workspace, w.work_off);
   return cuda_status(launch_permute(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -15,12 +15,22 @@
 //  - one elected thread per CTA drives a multi-stage shared-memory ring, so
 //    several row loads are in flight while earlier rows are stored;
 //  - the CTA's other warps zero its share of the gap rows with 16-byte
-//    stores and move the (small, 4-byte aligned) scale-factor rows;
-//  - gap rows are split evenly over CTAs by a prefix sum of gap sizes, so a
-//    hot expert with a big gap does not land on one CTA.
+//    stores; gap rows are split evenly over CTAs by a prefix sum of gap sizes.
+//
+// Two kernels:
+//  - permute_dyn_kernel (the default): a persistent grid, one wave at the
+//    occupancy the shared-memory ring allows, whose TMA threads claim tokens
+//    one at a time from a counter in the workspace.  A measured trace of the
+//    statically split kernel showed SMs with equal shares finishing as much
+//    as 40 % apart, and a grid of 1.3 waves when rows are small; claiming
+//    tokens keeps every SM busy to the end.  The token's slots and its scale
+//    factors come in by bulk copy on the same mbarrier as its row.
+//  - permute_kernel: a static split of contiguous token blocks, used when a
+//    row is wider than one 16 KiB slice or scale rows are not 16-byte sized.
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "launch.h"
@@ -41,18 +51,9 @@ constexpr int kPermuteWarps = kPermuteThreads / kWarpSize;
 constexpr int kMaxStages = 8;
 constexpr int kMaxChunkBytes = 16384;
 constexpr int kStageBudgetBytes = MOE_PERMUTE_STAGE_BUDGET;  // shared-memory ring per CTA
-constexpr int kCtasPerSm = MOE_PERMUTE_CTAS_PER_SM;           // grid sizing target
+constexpr int kCtasPerSm = MOE_PERMUTE_CTAS_PER_SM;           // static kernel's grid target
 constexpr int kMaxTokensPerCta = 512;
 constexpr int kSfRegWords = 4;  // scale-factor words a lane keeps in registers
-
-struct PermutePlan {
-  int chunk_bytes;     // bytes per bulk load (a row, or a 16 KiB slice of it)
-  int nchunks;         // slices per row
-  int stages;          // shared-memory ring depth
-  int tokens_per_cta;
-  int64_t grid;
-  size_t off_slots, off_active, off_padpre, smem;
-};
 
 __device__ __forceinline__ int warp_inclusive_scan(int v, int lane) {
 #pragma unroll
@@ -89,6 +90,46 @@ __device__ void gap_prefix(const int32_t* __restrict__ off, const int32_t* __res
   if (threadIdx.x == kPermuteThreads - 1) padpre[E] = run;
 }
 
+// This CTA's equal share of the gap rows (and their scale-factor rows) set to
+// zero by the nhelp threads htid = 0..nhelp-1.
+__device__ void zero_gap_share(const PermuteArgs& a, const int32_t* padpre_s, int E, int htid, int nhelp) {
+  const int64_t total_pad = padpre_s[E];
+  const int64_t G = gridDim.x;
+  const int64_t p0 = total_pad * blockIdx.x / G, p1 = total_pad * (blockIdx.x + 1) / G;
+  if (p0 >= p1) return;
+  // First expert whose gap holds pad index p0.
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) / 2;
+    if (padpre_s[mid] <= p0) lo = mid; else hi = mid - 1;
+  }
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  for (int e = lo; e < E && padpre_s[e] < p1; ++e) {
+    const int64_t a0 = max64(p0, padpre_s[e]), a1 = min64(p1, padpre_s[e + 1]);
+    if (a0 >= a1) continue;
+    const int64_t row0 = __ldg(a.expert_offset + e) + __ldg(a.expert_count + e) + (a0 - padpre_s[e]);
+    const int64_t nrows = a1 - a0;
+    uint8_t* base = a.recv_x + row0 * a.row_bytes;
+    const int64_t n16 = nrows * a.row_bytes / 16;
+    for (int64_t j = htid; j < n16; j += nhelp) ptx::st_cs_v4(base + j * 16, zero);
+    if (a.recv_sf) {
+      uint32_t* sb = reinterpret_cast<uint32_t*>(a.recv_sf + row0 * a.sf_row_bytes);
+      const int64_t nw = nrows * a.sf_row_bytes / 4;
+      for (int64_t j = htid; j < nw; j += nhelp) sb[j] = 0u;
+    }
+  }
+}
+
+// ------------------------------------------------------------ static split
+struct PermutePlan {
+  int chunk_bytes;     // bytes per bulk load (a row, or a 16 KiB slice of it)
+  int nchunks;         // slices per row
+  int stages;          // shared-memory ring depth
+  int tokens_per_cta;
+  int64_t grid;
+  size_t off_slots, off_active, off_padpre, smem;
+};
+
 __global__ void __launch_bounds__(kPermuteThreads)
     permute_kernel(const PermuteArgs a, const PermutePlan p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -115,13 +156,26 @@ __global__ void __launch_bounds__(kPermuteThreads)
     return;
   }
 
-  for (int i = threadIdx.x; i < ntok * K; i += kPermuteThreads) {
-    int s = __ldg(a.dst_slot + t0 * K + i);
-    if (s >= a.capacity) {
-      set_error(a.err, MOE_ERR_CAPACITY);
-      s = -1;
+  // Slots of the CTA's tokens; kBatch independent loads per thread in flight.
+  constexpr int kBatch = 8;
+  for (int base = threadIdx.x; base < ntok * K; base += kBatch * kPermuteThreads) {
+    int v[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = base + u * kPermuteThreads;
+      v[u] = i < ntok * K ? __ldg(a.dst_slot + t0 * K + i) : -1;
     }
-    slots_s[i] = s;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = base + u * kPermuteThreads;
+      if (i >= ntok * K) break;
+      int s = v[u];
+      if (s >= a.capacity) {
+        set_error(a.err, MOE_ERR_CAPACITY);
+        s = -1;
+      }
+      slots_s[i] = s;
+    }
   }
   if (a.zero_pad) gap_prefix(a.expert_offset, a.expert_count, E, padpre_s, warp_tot_s);
   __syncthreads();
@@ -157,6 +211,7 @@ __global__ void __launch_bounds__(kPermuteThreads)
     };
     const int prologue = min(S, units);
     for (int u = 0; u < prologue; ++u) issue(u);
+    int issued = prologue;
     int u = 0;
     bool ok = true;
     for (; u < units; ++u) {
@@ -177,12 +232,13 @@ __global__ void __launch_bounds__(kPermuteThreads)
       if (u + S < units) {
         ptx::bulk_wait_read<0>();  // this stage's stores have read it
         issue(u + S);
+        ++issued;
       }
     }
     if (!ok) {
       set_error(a.err, MOE_ERR_TIMEOUT);
       // Let the loads already issued land before the CTA's shared memory goes away.
-      for (int v = u; v < min(u + S, units); ++v)
+      for (int v = u; v < issued; ++v)
         ptx::mbar_wait_parity_bounded(&full_bar[v % S], (v / S) & 1, kWaitLimitNs);
     }
     ptx::bulk_wait<0>();
@@ -193,36 +249,7 @@ __global__ void __launch_bounds__(kPermuteThreads)
   const int htid = threadIdx.x - kWarpSize;
   const int nhelp = kPermuteThreads - kWarpSize;
   const int hwarp = warp - 1, nhwarps = kPermuteWarps - 1;
-
-  if (a.zero_pad) {
-    const int64_t total_pad = padpre_s[E];
-    const int64_t G = gridDim.x;
-    const int64_t p0 = total_pad * blockIdx.x / G, p1 = total_pad * (blockIdx.x + 1) / G;
-    if (p0 < p1) {
-      // First expert whose gap holds pad index p0.
-      int lo = 0, hi = E - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) / 2;
-        if (padpre_s[mid] <= p0) lo = mid; else hi = mid - 1;
-      }
-      const uint4 zero = make_uint4(0, 0, 0, 0);
-      for (int e = lo; e < E && padpre_s[e] < p1; ++e) {
-        const int64_t a0 = max64(p0, padpre_s[e]), a1 = min64(p1, padpre_s[e + 1]);
-        if (a0 >= a1) continue;
-        const int64_t row0 = __ldg(a.expert_offset + e) + __ldg(a.expert_count + e) + (a0 - padpre_s[e]);
-        const int64_t nrows = a1 - a0;
-        uint8_t* base = a.recv_x + row0 * a.row_bytes;
-        const int64_t n16 = nrows * a.row_bytes / 16;
-        for (int64_t j = htid; j < n16; j += nhelp) ptx::st_cs_v4(base + j * 16, zero);
-        if (a.recv_sf) {
-          uint32_t* sb = reinterpret_cast<uint32_t*>(a.recv_sf + row0 * a.sf_row_bytes);
-          const int64_t nw = nrows * a.sf_row_bytes / 4;
-          for (int64_t j = htid; j < nw; j += nhelp) sb[j] = 0u;
-        }
-      }
-    }
-  }
-
+  if (a.zero_pad) zero_gap_share(a, padpre_s, E, htid, nhelp);
   if (a.sf) {
     const int words = static_cast<int>(a.sf_row_bytes / 4);
     for (int tok = hwarp; tok < ntok; tok += nhwarps) {
@@ -276,9 +303,200 @@ PermutePlan make_permute_plan(const PermuteArgs& a, int sms) {
   return p;
 }
 
+// ------------------------------------------------------ dynamic (default)
+struct DynPlan {
+  int row_bytes;     // <= kMaxChunkBytes, multiple of 16
+  int slot_win;      // bytes reserved per stage for the token's 16-byte-aligned slot window
+  int sf_bytes;      // scale-factor row bytes (multiple of 16) or 0
+  int stage_bytes;   // row + slot window + scale row, rounded to 128
+  int stages;
+  int64_t grid;
+  size_t off_padpre, smem;
+};
+
+__global__ void __launch_bounds__(kPermuteThreads)
+    permute_dyn_kernel(const PermuteArgs a, const DynPlan p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages];
+  __shared__ int warp_tot_s[kPermuteWarps];
+  __shared__ int64_t stage_tok[kMaxStages];
+  int32_t* padpre_s = reinterpret_cast<int32_t*>(smem + p.off_padpre);
+  const int K = a.topk, E = a.num_experts;
+  const int warp = threadIdx.x / kWarpSize, lane = threadIdx.x % kWarpSize;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) ptx::mbar_init(&full_bar[s], 1);
+    ptx::fence_mbar_init();
+  }
+  ptx::grid_dependency_wait();
+  ptx::grid_dependency_launch_dependents();
+  const int64_t rows = __ldg(a.total_rows);
+  if (rows > a.capacity) {   // uniform over the grid: no CTA touches the token counter
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_error(a.err, MOE_ERR_CAPACITY);
+    return;
+  }
+  if (a.zero_pad) gap_prefix(a.expert_offset, a.expert_count, E, padpre_s, warp_tot_s);
+  __syncthreads();
+
+  if (warp != 0) {
+    if (a.zero_pad) zero_gap_share(a, padpre_s, E, threadIdx.x - kWarpSize, kPermuteThreads - kWarpSize);
+    return;
+  }
+  if (lane != 0) return;
+
+  // ---- the CTA's TMA thread ---------------------------------------------
+  const int64_t N = a.num_tokens;
+  const int64_t rb = a.row_bytes, srb = a.sf_row_bytes;
+  const int S = p.stages;
+  unsigned* next_tok = a.work;
+  unsigned* done_ctas = a.work + 1;
+  const uintptr_t slots_lo = reinterpret_cast<uintptr_t>(a.dst_slot);
+  const uintptr_t slots_hi = reinterpret_cast<uintptr_t>(a.dst_slot + N * K);
+  // 16-byte-aligned window of dst_slot holding token t's K slots; when it
+  // would reach outside the array the slots are read directly instead.
+  auto window_of = [&](int64_t t, uintptr_t& w0, uintptr_t& w1, uintptr_t& first) -> bool {
+    first = reinterpret_cast<uintptr_t>(a.dst_slot + t * K);
+    w0 = first & ~uintptr_t(15);
+    w1 = (first + 4u * static_cast<unsigned>(K) + 15) & ~uintptr_t(15);
+    return w0 >= slots_lo && w1 <= slots_hi;
+  };
+  // Claims run two tokens ahead of use, so the atomic's latency is hidden.
+  int64_t claim0 = atomicAdd(next_tok, 1u), claim1 = atomicAdd(next_tok, 1u);
+  bool exhausted = false;
+  int64_t issued = 0;
+  auto issue = [&]() {
+    const int64_t t = claim0;
+    claim0 = claim1;
+    if (t >= N) {
+      exhausted = true;
+      return;
+    }
+    claim1 = atomicAdd(next_tok, 1u);
+    const int s = static_cast<int>(issued % S);
+    uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
+    stage_tok[s] = t;
+    uintptr_t w0, w1, first;
+    const bool window = window_of(t, w0, w1, first);
+    const uint32_t tx = static_cast<uint32_t>(rb) + (window ? static_cast<uint32_t>(w1 - w0) : 0u) +
+                        static_cast<uint32_t>(p.sf_bytes);
+    ptx::mbar_arrive_expect_tx(&full_bar[s], tx);
+    ptx::bulk_g2s(st, a.x + t * rb, static_cast<uint32_t>(rb), &full_bar[s]);
+    if (window)
+      ptx::bulk_g2s(st + p.row_bytes, reinterpret_cast<const void*>(w0), static_cast<uint32_t>(w1 - w0),
+                    &full_bar[s]);
+    if (p.sf_bytes)
+      ptx::bulk_g2s(st + p.row_bytes + p.slot_win, a.sf + t * srb, static_cast<uint32_t>(p.sf_bytes), &full_bar[s]);
+    ++issued;
+  };
+  for (int i = 0; i < S && !exhausted; ++i) issue();
+  int64_t j = 0;
+  bool ok = true;
+  for (; j < issued; ++j) {
+    const int s = static_cast<int>(j % S);
+    if (!ptx::mbar_wait_parity_bounded(&full_bar[s], static_cast<uint32_t>((j / S) & 1), kWaitLimitNs)) {
+      ok = false;
+      break;
+    }
+    const int64_t t = stage_tok[s];
+    const uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
+    uintptr_t w0, w1, first;
+    const bool window = window_of(t, w0, w1, first);
+    const int32_t* sl = window ? reinterpret_cast<const int32_t*>(st + p.row_bytes + (first - w0)) : nullptr;
+    for (int k = 0; k < K; ++k) {
+      const int32_t slot = window ? sl[k] : __ldg(a.dst_slot + t * K + k);
+      if (slot < 0) continue;
+      if (slot >= a.capacity) {
+        set_error(a.err, MOE_ERR_CAPACITY);
+        continue;
+      }
+      ptx::bulk_s2g(a.recv_x + slot * rb, st, static_cast<uint32_t>(rb));
+      if (p.sf_bytes)
+        ptx::bulk_s2g(a.recv_sf + slot * srb, st + p.row_bytes + p.slot_win, static_cast<uint32_t>(srb));
+    }
+    ptx::bulk_commit();
+    if (!exhausted) {
+      ptx::bulk_wait_read<0>();  // this stage's stores have read it
+      issue();
+    }
+  }
+  if (!ok) {
+    set_error(a.err, MOE_ERR_TIMEOUT);
+    for (int64_t v = j; v < issued; ++v)
+      ptx::mbar_wait_parity_bounded(&full_bar[v % S], static_cast<uint32_t>((v / S) & 1), kWaitLimitNs);
+  }
+  ptx::bulk_wait<0>();
+  // The fence orders this CTA's claims before its arrival below; the last
+  // CTA to arrive resets both counters for the next launch on the workspace.
+  __threadfence();
+  if (atomicAdd(done_ctas, 1u) == gridDim.x - 1) {
+    atomicExch(next_tok, 0u);
+    atomicExch(done_ctas, 0u);
+  }
+}
+
+bool dyn_applicable(const PermuteArgs& a) {
+  if (a.row_bytes > kMaxChunkBytes || a.work == nullptr) return false;
+  if (a.sf != nullptr) {
+    if (a.sf_row_bytes % 16 != 0 || a.sf_row_bytes > 4096) return false;
+    if (reinterpret_cast<uintptr_t>(a.sf) % 16 != 0 || reinterpret_cast<uintptr_t>(a.recv_sf) % 16 != 0) return false;
+  }
+  return true;
+}
+
+DynPlan make_dyn_plan(const PermuteArgs& a) {
+  DynPlan p{};
+  p.row_bytes = static_cast<int>(a.row_bytes);
+  p.slot_win = static_cast<int>((4 * a.topk + 32 + 15) / 16 * 16);
+  p.sf_bytes = a.sf != nullptr ? static_cast<int>(a.sf_row_bytes) : 0;
+  p.stage_bytes = (p.row_bytes + p.slot_win + p.sf_bytes + 127) / 128 * 128;
+  p.stages = std::max(2, std::min(kMaxStages, kStageBudgetBytes / p.stage_bytes));
+  size_t off = static_cast<size_t>(p.stages) * p.stage_bytes;
+  p.off_padpre = off;
+  off += sizeof(int32_t) * (static_cast<size_t>(a.num_experts) + 1);
+  p.smem = (off + 127) / 128 * 128;
+  return p;
+}
+
+// CTAs of the dynamic kernel resident per SM at this shared-memory size (cached).
+int dyn_ctas_per_sm(size_t smem) {
+  static std::mutex mu;
+  static size_t cached_smem[8] = {};
+  static int cached_occ[8] = {};
+  static int cached_dev[8] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < 8; ++i)
+    if (cached_occ[i] > 0 && cached_smem[i] == smem && cached_dev[i] == dev) return cached_occ[i];
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, permute_dyn_kernel, kPermuteThreads, smem) != cudaSuccess ||
+      occ < 1)
+    occ = 1;
+  for (int i = 0; i < 8; ++i)
+    if (cached_occ[i] == 0) {
+      cached_smem[i] = smem;
+      cached_occ[i] = occ;
+      cached_dev[i] = dev;
+      break;
+    }
+  return occ;
+}
+
 }  // namespace
 
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t stream) {
+  if (dyn_applicable(a)) {
+    DynPlan p = make_dyn_plan(a);
+    cudaError_t st = cudaFuncSetAttribute(permute_dyn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(p.smem));
+    if (st != cudaSuccess) return st;
+    const int64_t resident = static_cast<int64_t>(dyn_ctas_per_sm(p.smem)) * device_sm_count();
+    p.grid = max64(1, min64(resident, a.num_tokens));
+    st = launch_pdl(permute_dyn_kernel, dim3(static_cast<unsigned>(p.grid)), dim3(kPermuteThreads), p.smem, stream,
+                    a, p);
+    if (st != cudaSuccess) return st;
+    count_launch();
+    return cudaSuccess;
+  }
   const PermutePlan p = make_permute_plan(a, device_sm_count());
   cudaError_t st = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(p.smem));

@@ -136,6 +136,17 @@ MOE_API int moe_layout_build(const moe_layout_desc* desc, const int64_t* topk_id
                              int32_t* total_rows, void* stream);
 
 /*
+ * moe_layout_build with int32 routing ids (topk_idx int32 [N*K]); same
+ * results.  Frameworks that keep top-k ids as int32 avoid a widening copy.
+ */
+MOE_API int moe_layout_build_i32(const moe_layout_desc* desc, const int32_t* topk_idx,
+                                 int32_t* expert_count, int32_t* rank_count,
+                                 void* workspace, size_t workspace_bytes,
+                                 int32_t* expert_offset, int32_t* rank_psum,
+                                 int32_t* dst_slot, int32_t* src_idx, int64_t capacity_rows,
+                                 int32_t* total_rows, void* stream);
+
+/*
  * Expand-mode dispatch permute ([CS] §6.3-§6.4, §8.2) with zero padding
  * ([CS] §7.3).  For every valid (t, k): recv_x row dst_slot[t*K+k] = x row t,
  * copied byte for byte (any row dtype: bf16, fp8, ...).  If sf is non-NULL

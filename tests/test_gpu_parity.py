@@ -356,3 +356,23 @@ def test_cumulative_expert_stats():
         binding.accumulate_stats(w, lay.expert_count, cum)
         want += oracle.layout(idx.numpy(), w.num_experts, w.num_ranks, w.alignment)["expert_count"]
     np.testing.assert_array_equal(cum.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("name", ["decode", "skewed", "roundtrip"])
+def test_int32_ids(name):
+    """moe_layout_build_i32: int32 routing ids give the int64 path's layout."""
+    w = wl.WORKLOADS[name]
+    idx = wl.draw_topk_idx(w, 3)
+    ref = oracle.layout(idx.numpy(), w.num_experts, w.num_ranks, w.alignment)
+    lay = binding.Layout(w, wl.worst_case_rows(w), device=DEV).build(idx.to(torch.int32).to(DEV))
+    assert lay.error() == 0
+    assert_layout_matches(lay, ref, w)
+
+
+def test_int32_ids_separate_kernels():
+    w = _w(200000, 32, 64, 4, 16, H=16)             # more tiles than fit at once: three-kernel path
+    idx = wl.draw_topk_idx(w, 32)
+    ref = oracle.layout(idx.numpy(), 64, 4, 16)
+    lay = binding.Layout(w, wl.worst_case_rows(w), device=DEV).build(idx.to(torch.int32).to(DEV))
+    assert lay.error() == 0
+    assert_layout_matches(lay, ref, w)
