@@ -41,8 +41,8 @@ L2_FLUSH_BYTES = 256 << 20          # > 2x the 129 MB L2
 # DRAM traffic of the permute kernel from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), per launch, scaled to the decode workload, tied to
 # the kernel sources it was measured on.  bench reports null if they changed.
-PERMUTE_TRAFFIC = {"sha256": "82ea9003edeb54802d788183e1902ed93f73deb938f61a48206bdbea331f877e",
-                   "workload": "decode", "bytes_per_launch": 58_980_352 + 646_405_888}
+PERMUTE_TRAFFIC = {"sha256": "78e49d470fbe4630e851b31cfd7452435e1b5bec1d43ac7675a112b40573dd5a",
+                   "workload": "decode", "bytes_per_launch": 58_954_240 + 646_191_872}
 PERMUTE_SOURCES = ["counting_sort_bucketization_gb300/csrc/permute_kernel.cu",
                    "counting_sort_bucketization_gb300/csrc/ptx.cuh",
                    "counting_sort_bucketization_gb300/csrc/common.cuh"]
@@ -367,7 +367,7 @@ def run_native(args, rank, world, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(w),
-        "roofline": {"kernel": "permute_kernel", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+        "roofline": {"kernel": "permute_dyn_kernel", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "peak_source": peaks["source"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "traffic": traffic, "algorithmic_bytes_per_launch": ab["permute"]},
         "kernels_ms": {"layout": kern_ms[0], "permute": kern_ms[1], "combine": kern_ms[2]},

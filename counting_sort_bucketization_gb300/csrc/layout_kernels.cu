@@ -131,62 +131,39 @@ __device__ void count_phase(const TilePlan& plan, int K, int E, int R, int tile,
 // Every row becomes an exclusive prefix over tiles (in place); expert rows
 // give expert_count, rank rows rank_count.  Loads go through L2 (__ldcg): in the fused
 // kernel other CTAs wrote these rows earlier in the same launch.
-constexpr int kScanRegChunks = 8;   // rows of up to 8 x 32 tiles are scanned from registers
+constexpr int kScanBatch = 8;   // 32-tile chunks of a row loaded before they are scanned
 
 __device__ void scan_phase(int32_t* __restrict__ hist, int32_t* __restrict__ rhist, int64_t T, int E,
                            int R, int32_t* __restrict__ expert_count, int32_t* __restrict__ rank_count) {
   const int warp = threadIdx.x / kWarpSize, lane = threadIdx.x % kWarpSize;
-  const int64_t m = ceil_div64(T, kWarpSize);
-  const int64_t lo = min64(lane * m, T), hi = min64(lo + m, T);
   for (int row = blockIdx.x * kLayoutWarps + warp; row < E + R; row += gridDim.x * kLayoutWarps) {
     const bool is_expert = row < E;
-    const int32_t* src = is_expert ? hist + static_cast<int64_t>(row) * T
-                                   : rhist + static_cast<int64_t>(row - E) * T;
-    if (T <= kWarpSize * kScanRegChunks) {
-      // All loads first (coalesced, 32 tiles per load), then one warp scan per
-      // 32-tile chunk with a running carry: one L2 round trip per row.
-      int v[kScanRegChunks];
+    int32_t* col = is_expert ? hist + static_cast<int64_t>(row) * T : rhist + static_cast<int64_t>(row - E) * T;
+    // kScanBatch coalesced loads (32 tiles each) in flight, then one warp scan
+    // per 32-tile chunk with a running carry; the row becomes an exclusive
+    // prefix in place.
+    int carry = 0;
+    for (int64_t base = 0; base < T; base += kScanBatch * kWarpSize) {
+      int v[kScanBatch];
 #pragma unroll
-      for (int j = 0; j < kScanRegChunks; ++j) {
-        const int64_t i = j * kWarpSize + lane;
-        v[j] = i < T ? __ldcg(src + i) : 0;
+      for (int j = 0; j < kScanBatch; ++j) {
+        const int64_t i = base + j * kWarpSize + lane;
+        v[j] = i < T ? __ldcg(col + i) : 0;
       }
-      int carry = 0;
-      int32_t* dst = const_cast<int32_t*>(src);
 #pragma unroll
-      for (int j = 0; j < kScanRegChunks; ++j) {
-        if (j * kWarpSize >= T) break;
+      for (int j = 0; j < kScanBatch; ++j) {
+        if (base + j * kWarpSize >= T) break;
         const int incl = warp_inclusive_scan(v[j], lane);
-        const int64_t i = j * kWarpSize + lane;
-        if (i < T) dst[i] = carry + incl - v[j];
+        const int64_t i = base + j * kWarpSize + lane;
+        if (i < T) col[i] = carry + incl - v[j];
         carry += __shfl_sync(kFull, incl, kWarpSize - 1);
       }
-      if (lane == 0) {
-        if (is_expert)
-          expert_count[row] = carry;
-        else
-          rank_count[row - E] = carry;
-      }
-      continue;
-    }
-    // Longer rows: each lane sums a contiguous run, warp scan of the run sums,
-    // then each lane rewrites its run.
-    int sum = 0;
-    for (int64_t i = lo; i < hi; ++i) sum += __ldcg(src + i);
-    const int incl = warp_inclusive_scan(sum, lane);
-    const int total = __shfl_sync(kFull, incl, kWarpSize - 1);
-    int32_t* dst = const_cast<int32_t*>(src);
-    int run = incl - sum;
-    for (int64_t i = lo; i < hi; ++i) {
-      const int c = __ldcg(dst + i);
-      dst[i] = run;
-      run += c;
     }
     if (lane == 0) {
       if (is_expert)
-        expert_count[row] = total;
+        expert_count[row] = carry;
       else
-        rank_count[row - E] = total;
+        rank_count[row - E] = carry;
     }
   }
 }

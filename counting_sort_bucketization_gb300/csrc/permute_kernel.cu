@@ -90,6 +90,36 @@ __device__ void gap_prefix(const int32_t* __restrict__ off, const int32_t* __res
   if (threadIdx.x == kPermuteThreads - 1) padpre[E] = run;
 }
 
+// gap_prefix computed by the helper warps alone (threads kWarpSize.., a named
+// barrier instead of __syncthreads), so warp 0 never waits for it.
+__device__ void gap_prefix_helpers(const int32_t* __restrict__ off, const int32_t* __restrict__ cnt, int E,
+                                   int32_t* padpre, int* warp_tot) {
+  constexpr int kHelp = kPermuteThreads - kWarpSize;
+  const int h = threadIdx.x - kWarpSize;
+  const int lane = h % kWarpSize, hw = h / kWarpSize;
+  const int ipt = (E + kHelp - 1) / kHelp;
+  const int e_lo = h * ipt;
+  int mine = 0;
+  for (int j = 0; j < ipt; ++j) {
+    const int e = e_lo + j;
+    if (e < E) mine += __ldg(off + e + 1) - __ldg(off + e) - __ldg(cnt + e);
+  }
+  const int incl = warp_inclusive_scan(mine, lane);
+  if (lane == kWarpSize - 1) warp_tot[hw] = incl;
+  asm volatile("bar.sync 1, %0;" ::"r"(kHelp) : "memory");
+  int run = incl - mine;
+  for (int w = 0; w < hw; ++w) run += warp_tot[w];
+  for (int j = 0; j < ipt; ++j) {
+    const int e = e_lo + j;
+    if (e < E) {
+      padpre[e] = run;
+      run += __ldg(off + e + 1) - __ldg(off + e) - __ldg(cnt + e);
+    }
+  }
+  if (h == kHelp - 1) padpre[E] = run;
+  asm volatile("bar.sync 1, %0;" ::"r"(kHelp) : "memory");
+}
+
 // This CTA's equal share of the gap rows (and their scale-factor rows) set to
 // zero by the nhelp threads htid = 0..nhelp-1.
 __device__ void zero_gap_share(const PermuteArgs& a, const int32_t* padpre_s, int E, int htid, int nhelp) {
@@ -323,22 +353,13 @@ __global__ void __launch_bounds__(kPermuteThreads)
   int32_t* padpre_s = reinterpret_cast<int32_t*>(smem + p.off_padpre);
   const int K = a.topk, E = a.num_experts;
   const int warp = threadIdx.x / kWarpSize, lane = threadIdx.x % kWarpSize;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < p.stages; ++s) ptx::mbar_init(&full_bar[s], 1);
-    ptx::fence_mbar_init();
-  }
-  ptx::grid_dependency_wait();
-  ptx::grid_dependency_launch_dependents();
-  const int64_t rows = __ldg(a.total_rows);
-  if (rows > a.capacity) {   // uniform over the grid: no CTA touches the token counter
-    if (blockIdx.x == 0 && threadIdx.x == 0) set_error(a.err, MOE_ERR_CAPACITY);
-    return;
-  }
-  if (a.zero_pad) gap_prefix(a.expert_offset, a.expert_count, E, padpre_s, warp_tot_s);
-  __syncthreads();
 
   if (warp != 0) {
-    if (a.zero_pad) zero_gap_share(a, padpre_s, E, threadIdx.x - kWarpSize, kPermuteThreads - kWarpSize);
+    // Helper warps: this CTA's share of the gap rows, after the layout is done.
+    ptx::grid_dependency_wait();
+    if (__ldg(a.total_rows) > a.capacity || !a.zero_pad) return;
+    gap_prefix_helpers(a.expert_offset, a.expert_count, E, padpre_s, warp_tot_s);
+    zero_gap_share(a, padpre_s, E, threadIdx.x - kWarpSize, kPermuteThreads - kWarpSize);
     return;
   }
   if (lane != 0) return;
@@ -347,6 +368,7 @@ __global__ void __launch_bounds__(kPermuteThreads)
   const int64_t N = a.num_tokens;
   const int64_t rb = a.row_bytes, srb = a.sf_row_bytes;
   const int S = p.stages;
+  const int64_t G = gridDim.x;
   unsigned* next_tok = a.work;
   unsigned* done_ctas = a.work + 1;
   const uintptr_t slots_lo = reinterpret_cast<uintptr_t>(a.dst_slot);
@@ -359,10 +381,51 @@ __global__ void __launch_bounds__(kPermuteThreads)
     w1 = (first + 4u * static_cast<unsigned>(K) + 15) & ~uintptr_t(15);
     return w0 >= slots_lo && w1 <= slots_hi;
   };
-  // Claims run two tokens ahead of use, so the atomic's latency is hidden.
-  int64_t claim0 = atomicAdd(next_tok, 1u), claim1 = atomicAdd(next_tok, 1u);
-  bool exhausted = false;
-  int64_t issued = 0;
+  for (int s = 0; s < S; ++s) ptx::mbar_init(&full_bar[s], 1);
+  ptx::fence_mbar_init();
+
+  // The first S tokens of every CTA are fixed (blockIdx.x + i*G): their rows
+  // and scale rows do not depend on the layout, so they are requested before
+  // waiting for the previous kernel.  Each stage's phase completes only after
+  // the post-wait arrival, which also brings the slot window.
+  int npre = 0;
+  for (; npre < S; ++npre) {
+    const int64_t t = blockIdx.x + npre * G;
+    if (t >= N) break;
+    uint8_t* st = smem + static_cast<size_t>(npre) * p.stage_bytes;
+    stage_tok[npre] = t;
+    ptx::mbar_expect_tx(&full_bar[npre], static_cast<uint32_t>(rb + p.sf_bytes));
+    ptx::bulk_g2s(st, a.x + t * rb, static_cast<uint32_t>(rb), &full_bar[npre]);
+    if (p.sf_bytes)
+      ptx::bulk_g2s(st + p.row_bytes + p.slot_win, a.sf + t * srb, static_cast<uint32_t>(p.sf_bytes),
+                    &full_bar[npre]);
+  }
+  ptx::grid_dependency_wait();
+  ptx::grid_dependency_launch_dependents();
+  const bool cap_ok = __ldg(a.total_rows) <= a.capacity;   // uniform over the grid
+  if (!cap_ok) {
+    if (blockIdx.x == 0) set_error(a.err, MOE_ERR_CAPACITY);
+    for (int i = 0; i < npre; ++i) ptx::mbar_arrive(&full_bar[i]);
+    for (int i = 0; i < npre; ++i) ptx::mbar_wait_parity_bounded(&full_bar[i], 0, kWaitLimitNs);
+    return;   // no CTA touches the token counter
+  }
+  for (int i = 0; i < npre; ++i) {
+    uintptr_t w0, w1, first;
+    if (window_of(stage_tok[i], w0, w1, first)) {
+      ptx::mbar_arrive_expect_tx(&full_bar[i], static_cast<uint32_t>(w1 - w0));
+      ptx::bulk_g2s(smem + static_cast<size_t>(i) * p.stage_bytes + p.row_bytes, reinterpret_cast<const void*>(w0),
+                    static_cast<uint32_t>(w1 - w0), &full_bar[i]);
+    } else {
+      ptx::mbar_arrive(&full_bar[i]);
+    }
+  }
+
+  // Later tokens are claimed from the counter (claim c is token G*S + c),
+  // two claims ahead of use so the atomic's latency is hidden.
+  const int64_t claimed_base = G * S;
+  int64_t claim0 = claimed_base + atomicAdd(next_tok, 1u), claim1 = claimed_base + atomicAdd(next_tok, 1u);
+  bool exhausted = npre < S;
+  int64_t issued = npre;
   auto issue = [&]() {
     const int64_t t = claim0;
     claim0 = claim1;
@@ -370,7 +433,7 @@ __global__ void __launch_bounds__(kPermuteThreads)
       exhausted = true;
       return;
     }
-    claim1 = atomicAdd(next_tok, 1u);
+    claim1 = claimed_base + atomicAdd(next_tok, 1u);
     const int s = static_cast<int>(issued % S);
     uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
     stage_tok[s] = t;
@@ -387,7 +450,6 @@ __global__ void __launch_bounds__(kPermuteThreads)
       ptx::bulk_g2s(st + p.row_bytes + p.slot_win, a.sf + t * srb, static_cast<uint32_t>(p.sf_bytes), &full_bar[s]);
     ++issued;
   };
-  for (int i = 0; i < S && !exhausted; ++i) issue();
   int64_t j = 0;
   bool ok = true;
   for (; j < issued; ++j) {

@@ -79,10 +79,12 @@ typedef struct moe_layout_desc {
 
 /*
  * Bytes of device workspace the other calls need for this description
- * (sticky error word, per-tile expert and rank histograms).  The workspace
- * must be zero-filled once before its first use (e.g. cudaMemsetAsync);
- * afterwards the calls keep it consistent.  One workspace serves one stream
- * at a time.
+ * (sticky error word, grid-barrier words, the permute's work counter,
+ * per-tile expert and rank histograms).  The workspace must
+ * be zero-filled once before its first use (e.g. cudaMemsetAsync);
+ * afterwards every call leaves it ready for the next.  One workspace serves
+ * one stream at a time: calls that overlap on the GPU must not share it.
+ * After MOE_ERR_TIMEOUT, zero-fill it again.
  */
 MOE_API int moe_layout_workspace_bytes(const moe_layout_desc* desc, size_t* bytes);
 
