@@ -184,9 +184,47 @@ struct RankArgs {
   int* err;
 };
 
-// ids_s holds the tile's staged ids; off_s [E+1], cnt_s [kLayoutWarps*E]
-// (zeroed), lr_s [tile pairs] are shared scratch.
-__device__ void rank_phase(const TilePlan& plan, const RankArgs& a, int tile, TileCoords tc, const int* ids_s,
+// Rank of each pair among the same expert's pairs earlier in its warp's run
+// (lr_s), and each warp's per-expert counts (cnt_s[warp][e], zeroed before).
+// When rhist_s is given, also the tile's rank counts, once per token and
+// rank ([CS] §4.2 deduplication): the fused kernel needs no separate count pass.
+__device__ void rank_pass(const TilePlan& plan, int K, int E, int R, int ntok, const int* ids_s, int* cnt_s,
+                          int* lr_s, int* rhist_s) {
+  const int warp = threadIdx.x / kWarpSize, lane = threadIdx.x % kWarpSize;
+  const int L = E / R;
+  const int tok_in_chunk = lane / K;
+  int* my_cnt = cnt_s + warp * E;
+  for (int c = 0; c < plan.cpw; ++c) {
+    const int chunk = warp * plan.cpw + c;
+    const int tok = chunk * plan.tpc + tok_in_chunk;
+    const bool in = lane < plan.lanes && tok < ntok;
+    const int pair = chunk * plan.lanes + lane;
+    const int e = in ? ids_s[pair] : -1;
+    const bool valid = e >= 0;
+    const unsigned peers = __match_any_sync(kFull, valid ? static_cast<unsigned>(e)
+                                                         : (0x80000000u | lane));
+    const int base = valid ? my_cnt[e] : 0;
+    __syncwarp();
+    if (valid) {
+      if (__ffs(peers) - 1 == lane) my_cnt[e] = base + __popc(peers);
+      lr_s[pair] = base + __popc(peers & ptx::lanemask_lt());
+    }
+    __syncwarp();
+    if (rhist_s != nullptr) {
+      const int r = valid ? e / L : 0;
+      const unsigned rkey = valid ? static_cast<unsigned>(tok_in_chunk * MOE_MAX_EXPERTS + r)
+                                  : (0x80000000u | lane);
+      const unsigned rpeers = __match_any_sync(kFull, rkey);
+      if (valid && __ffs(rpeers) - 1 == lane) atomicAdd(&rhist_s[r], 1);
+    }
+  }
+  __syncthreads();
+}
+
+// ids_s holds the tile's staged ids; cnt_s [kLayoutWarps*E] and lr_s come
+// from rank_pass; off_s [E+1] is shared scratch.  Offsets, the tile-0
+// outputs, absolute slots, the maps and the gap rows of src_idx.
+__device__ void rank_finish(const TilePlan& plan, const RankArgs& a, int tile, TileCoords tc, const int* ids_s,
                            int* off_s, int* cnt_s, int* lr_s, int* warp_tot_s) {
   const int K = a.K, E = a.E, R = a.R, A = a.A;
   const int64_t T = plan.tiles;
@@ -250,28 +288,6 @@ __device__ void rank_phase(const TilePlan& plan, const RankArgs& a, int tile, Ti
     }
   }
 
-  // Rank of each pair among the same expert's pairs earlier in its warp's run.
-  const int tok_in_chunk = lane / K;
-  int* my_cnt = cnt_s + warp * E;
-  for (int c = 0; c < plan.cpw; ++c) {
-    const int chunk = warp * plan.cpw + c;
-    const int tok = chunk * plan.tpc + tok_in_chunk;
-    const bool in = lane < plan.lanes && tok < tc.ntok;
-    const int pair = chunk * plan.lanes + lane;
-    const int e = in ? ids_s[pair] : -1;
-    const bool valid = e >= 0;
-    const unsigned peers = __match_any_sync(kFull, valid ? static_cast<unsigned>(e)
-                                                         : (0x80000000u | lane));
-    const int base = valid ? my_cnt[e] : 0;
-    __syncwarp();
-    if (valid) {
-      if (__ffs(peers) - 1 == lane) my_cnt[e] = base + __popc(peers);
-      lr_s[pair] = base + __popc(peers & ptx::lanemask_lt());
-    }
-    __syncwarp();
-  }
-  __syncthreads();
-
   // Per expert: turn the per-warp counts into absolute slot bases.
 #pragma unroll
   for (int j = 0; j < kPerThread; ++j) {
@@ -306,6 +322,12 @@ __device__ void rank_phase(const TilePlan& plan, const RankArgs& a, int tile, Ti
       for (int row = lo + threadIdx.x; row < hi; row += blockDim.x) a.src_idx[row] = -1;
     }
   }
+}
+
+__device__ void rank_phase(const TilePlan& plan, const RankArgs& a, int tile, TileCoords tc, const int* ids_s,
+                           int* off_s, int* cnt_s, int* lr_s, int* warp_tot_s) {
+  rank_pass(plan, a.K, a.E, a.R, tc.ntok, ids_s, cnt_s, lr_s, nullptr);
+  rank_finish(plan, a, tile, tc, ids_s, off_s, cnt_s, lr_s, warp_tot_s);
 }
 
 // ---------------------------------------------------------- kernels
@@ -350,6 +372,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
   ptx::grid_dependency_wait();
   ptx::grid_dependency_launch_dependents();
   stage_tile_ids(topk_idx, tc.t0 * a.K, tc.ntok * a.K, a.E, ids_s, a.err);
+  __syncthreads();   // staged ids and zeroed counters visible to every warp
   rank_phase(plan, a, blockIdx.x, tc, ids_s, off_s, cnt_s, lr_s, warp_tot_s);
 }
 
@@ -392,25 +415,34 @@ __global__ void __launch_bounds__(kLayoutThreads)
   const int E = a.E, R = a.R, K = a.K;
   int* ids_s = smem;                            // [tile pairs], kept across all phases
   int* lr_s = ids_s + plan.tile_tokens * K;     // [tile pairs]
-  int* cnt_s = lr_s + plan.tile_tokens * K;     // [kLayoutWarps][E]; its first E + R ints
-                                                // serve as the count phase's histograms
+  int* cnt_s = lr_s + plan.tile_tokens * K;     // [kLayoutWarps][E]
   int* off_s = cnt_s + kLayoutWarps * E;        // [E+1]
+  int* rhist_s = off_s + (E + 1);               // [R]
   __shared__ int warp_tot_s[kLayoutWarps];
   __shared__ int flag_s;
-  const TileCoords tc = tile_coords(plan, a.N, blockIdx.x);
-  int* hist_s = cnt_s;
-  int* rhist_s = cnt_s + E;
-  for (int i = threadIdx.x; i < E + R; i += blockDim.x) hist_s[i] = 0;
+  const int tile = blockIdx.x;
+  const int64_t T = plan.tiles;
+  const TileCoords tc = tile_coords(plan, a.N, tile);
+  for (int i = threadIdx.x; i < kLayoutWarps * E; i += blockDim.x) cnt_s[i] = 0;
+  for (int i = threadIdx.x; i < R; i += blockDim.x) rhist_s[i] = 0;
   ptx::grid_dependency_wait();
   ptx::grid_dependency_launch_dependents();
   stage_tile_ids(topk_idx, tc.t0 * K, tc.ntok * K, E, ids_s, a.err);
   __syncthreads();
-  count_phase(plan, K, E, R, blockIdx.x, tc.ntok, ids_s, hist_s, rhist_s, hist, rhist);
+  // One pass over the tile's pairs: ranks inside each warp's run, per-warp
+  // expert counts, deduplicated rank counts.  The tile's expert count is the
+  // sum of the per-warp counts.
+  rank_pass(plan, K, E, R, tc.ntok, ids_s, cnt_s, lr_s, rhist_s);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int c = 0;
+    for (int w = 0; w < kLayoutWarps; ++w) c += cnt_s[w * E + e];
+    hist[static_cast<int64_t>(e) * T + tile] = c;
+  }
+  for (int r = threadIdx.x; r < R; r += blockDim.x) rhist[static_cast<int64_t>(r) * T + tile] = rhist_s[r];
   if (!grid_barrier(bar, bar + 1, gridDim.x, a.err, &flag_s)) return;
   scan_phase(hist, rhist, plan.tiles, E, R, expert_count, rank_count);
-  for (int i = threadIdx.x; i < kLayoutWarps * E; i += blockDim.x) cnt_s[i] = 0;
   if (!grid_barrier(bar, bar + 1, gridDim.x, a.err, &flag_s)) return;
-  rank_phase(plan, a, blockIdx.x, tc, ids_s, off_s, cnt_s, lr_s, warp_tot_s);
+  rank_finish(plan, a, tile, tc, ids_s, off_s, cnt_s, lr_s, warp_tot_s);
 }
 
 // ------------------------------------------- non-expand rank rows
@@ -547,7 +579,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
 size_t fused_smem_bytes(const moe_layout_desc& d, const TilePlan& p) {
   const size_t pairs = static_cast<size_t>(p.tile_tokens) * d.topk;
   const size_t E = d.num_experts;
-  return sizeof(int) * (2 * pairs + kLayoutWarps * E + E + 1);
+  return sizeof(int) * (2 * pairs + kLayoutWarps * E + E + 1 + d.num_ranks);
 }
 
 // Whether every tile's CTA of the fused kernel can be resident at once.
