@@ -370,7 +370,7 @@ def run_native(args, rank, world, local):
         "roofline": {"kernel": "permute_dyn_kernel", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "peak_source": peaks["source"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "traffic": traffic, "algorithmic_bytes_per_launch": ab["permute"]},
-        "kernels_ms": {"layout": kern_ms[0], "permute": kern_ms[1], "combine": kern_ms[2]},
+        "kernels_ms": {"layout": kern_ms[0], "permute": kern_ms[1], "combine": kern_ms[2] if do_combine else None},
         "kernels_gbs": {"permute": ab["permute"] / permute_s / 1e9,
                         "combine": (ab["combine"] / (kern_ms[2] / 1e3) / 1e9) if do_combine else None},
         "dispatch_tokens_per_s": world * N / (dispatch_ms / 1e3),
