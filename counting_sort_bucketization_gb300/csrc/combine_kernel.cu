@@ -18,6 +18,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "launch.h"
@@ -26,14 +27,20 @@
 namespace moe {
 namespace {
 
-#ifndef MOE_COMBINE_CTAS_PER_SM
-#define MOE_COMBINE_CTAS_PER_SM 8
+// Grid = this many full waves at the kernel's occupancy (a grid of 1.7 waves
+// left a third of the SMs idle during the partial second wave).
+#ifndef MOE_COMBINE_WAVES
+#define MOE_COMBINE_WAVES 2
 #endif
 
 constexpr int kCombineThreads = 256;
 constexpr int kKGroup = 8;              // expert rows loaded before their FMAs
 constexpr int kMaxTokensPerCta = 64;
-constexpr int kCtasPerSm = MOE_COMBINE_CTAS_PER_SM;   // grid sizing target
+constexpr int kWaves = MOE_COMBINE_WAVES;
+#ifndef MOE_COMBINE_VEC_UNROLL
+#define MOE_COMBINE_VEC_UNROLL 1
+#endif
+constexpr int kVecUnroll = MOE_COMBINE_VEC_UNROLL;
 
 __device__ __forceinline__ void fma_bf16x8(float (&acc)[8], float w, const uint4& v) {
   const uint32_t u[4] = {v.x, v.y, v.z, v.w};
@@ -93,40 +100,69 @@ __global__ void __launch_bounds__(kCombineThreads)
     const int32_t* sl = slot_s + tt * K;
     const float* wt = w_s + tt * K;
     uint16_t* orow = a.out + (t0 + tt) * H;
-    for (int j = threadIdx.x; j < nvec; j += kCombineThreads) {
-      float acc[8];
+    // kVecUnroll column vectors per thread per pass, all their row loads in
+    // flight before the FMAs.
+    for (int j0 = threadIdx.x; j0 < nvec; j0 += kVecUnroll * kCombineThreads) {
+      float acc[kVecUnroll][8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+      for (int x = 0; x < kVecUnroll; ++x)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[x][i] = 0.0f;
       for (int kg = 0; kg < K; kg += kKGroup) {
-        uint4 v[kKGroup];
+        uint4 v[kVecUnroll][kKGroup];
 #pragma unroll
-        for (int q = 0; q < kKGroup; ++q) {
-          const int k = kg + q;
-          const int32_t s = k < K ? sl[k] : -1;
-          v[q] = s >= 0 ? ptx::ld_nc_v4(a.expert_out + static_cast<int64_t>(s) * H + j * 8)
-                        : make_uint4(0, 0, 0, 0);
+        for (int x = 0; x < kVecUnroll; ++x) {
+          const int j = j0 + x * kCombineThreads;
+#pragma unroll
+          for (int q = 0; q < kKGroup; ++q) {
+            const int k = kg + q;
+            const int32_t s = (k < K && j < nvec) ? sl[k] : -1;
+            v[x][q] = s >= 0 ? ptx::ld_nc_v4(a.expert_out + static_cast<int64_t>(s) * H + j * 8)
+                             : make_uint4(0, 0, 0, 0);
+          }
         }
 #pragma unroll
-        for (int q = 0; q < kKGroup; ++q) {
-          const int k = kg + q;
-          if (k < K && sl[k] >= 0) fma_bf16x8(acc, wt[k], v[q]);
-        }
+        for (int x = 0; x < kVecUnroll; ++x)
+#pragma unroll
+          for (int q = 0; q < kKGroup; ++q) {
+            const int k = kg + q;
+            if (k < K && sl[k] >= 0) fma_bf16x8(acc[x], wt[k], v[x][q]);
+          }
       }
-      uint4 o;
-      o.x = pack_bf16x2(acc[0], acc[1]);
-      o.y = pack_bf16x2(acc[2], acc[3]);
-      o.z = pack_bf16x2(acc[4], acc[5]);
-      o.w = pack_bf16x2(acc[6], acc[7]);
-      ptx::st_v4(orow + j * 8, o);
+#pragma unroll
+      for (int x = 0; x < kVecUnroll; ++x) {
+        const int j = j0 + x * kCombineThreads;
+        if (j >= nvec) break;
+        uint4 o;
+        o.x = pack_bf16x2(acc[x][0], acc[x][1]);
+        o.y = pack_bf16x2(acc[x][2], acc[x][3]);
+        o.z = pack_bf16x2(acc[x][4], acc[x][5]);
+        o.w = pack_bf16x2(acc[x][6], acc[x][7]);
+        ptx::st_v4(orow + j * 8, o);
+      }
     }
   }
+}
+
+int combine_ctas_per_sm() {
+  static int occ = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    const size_t smem = (sizeof(int32_t) + sizeof(float)) * kMaxTokensPerCta * MOE_MAX_TOPK;
+    if (cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, combine_kernel, kCombineThreads, smem) != cudaSuccess ||
+        occ < 1)
+      occ = 1;
+  });
+  return occ;
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
   const int sms = device_sm_count();
-  const int64_t target_ctas = static_cast<int64_t>(kCtasPerSm) * sms;
+  const int64_t target_ctas = static_cast<int64_t>(kWaves) * combine_ctas_per_sm() * sms;
   int64_t tpc = ceil_div64(max64(a.num_tokens, 1), target_ctas);
   tpc = max64(1, min64(tpc, kMaxTokensPerCta));
   const int64_t grid = max64(1, ceil_div64(a.num_tokens, tpc));
