@@ -234,6 +234,38 @@ def algorithmic_bytes(w: wl.Workload, lay) -> dict:
             "tokens_routed": n_tok}
 
 
+def run_layout_only(args, local):
+    """Time the layout step alone (ids in, maps out): small on the device at any
+    workload size, so it is also the command to profile the layout kernels with."""
+    from counting_sort_bucketization_gb300 import binding
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = wl.WORKLOADS[args.workload]
+    idx = wl.draw_topk_idx(w, wl.SEEDS[w.name]).to(dev)
+    lay = binding.Layout(w, wl.worst_case_rows(w), device=dev)
+    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    times = {}
+    for fused in (True, False):
+        evs = []
+        for i in range(args.warmup + args.steps):
+            flush_w.zero_()
+            flush_r.max()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            lay.build(idx, fused=fused)
+            b.record()
+            if i >= args.warmup:
+                evs.append((a, b))
+        torch.cuda.synchronize(dev)
+        times["one_call" if fused else "two_calls"] = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    assert lay.error() == 0
+    print(json.dumps({"mode": "layout-only", "config": config_of(w), "steps": args.steps, "warmup": args.warmup,
+                      "layout_ms": times, "tokens_per_s": {k: w.num_tokens / (v / 1e3) for k, v in times.items()}}),
+          flush=True)
+
+
 def run_native(args, rank, world, local):
     from counting_sort_bucketization_gb300 import binding
 
@@ -445,6 +477,8 @@ def parse_args(argv=None):
     ap.add_argument("--ref-seconds", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--layout-only", action="store_true",
+                    help="time only the layout step (count, scan, maps) on the chosen workload")
     return ap.parse_args(argv)
 
 
@@ -456,6 +490,9 @@ def main(argv=None):
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.layout_only:
+        if rank == 0:
+            run_layout_only(args, local)
     else:
         run_native(args, rank, world, local)
     if world > 1 and torch.distributed.is_initialized():
