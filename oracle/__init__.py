@@ -71,6 +71,8 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.oracle_permute.restype = ctypes.c_int
     lib.oracle_permute.argtypes = [i64, i32, p, p, i64, p, i64, i32, p, p, p, p, i64, i32]
     lib.oracle_f32_to_bf16.restype = None
+    lib.oracle_permute_sf_col_major.argtypes = [i64, i32, p, p, i64, i32, p, p, p, i64, i64, i32]
+    lib.oracle_permute_sf_col_major.restype = ctypes.c_int
     lib.oracle_f32_to_bf16.argtypes = [i64, p, p]
     lib.oracle_expert_scale.restype = None
     lib.oracle_expert_scale.argtypes = [i64, i64, p, i32, p, p, p]
@@ -166,6 +168,27 @@ def permute(x_bytes: np.ndarray, dst_slot, expert_offset, expert_count, rows: in
     st = lib.oracle_permute(N, K, _ptr(dst), _ptr(x), rb, _ptr(sf), srb or 0, E, _ptr(off),
                             _ptr(cnt), _ptr(recv), _ptr(recv_sf), rows, 1 if zero_pad else 0)
     return int(st), recv, recv_sf
+
+
+def permute_sf_col_major(sf_words: np.ndarray, dst_slot, expert_offset, expert_count, rows: int,
+                         ld: int | None = None, zero_pad: bool = True, lib: ctypes.CDLL | None = None):
+    """Scale factors of the receive buffer, column-major: ``sf_words`` is
+    uint32 [N, C] (fp32 scales viewed as words); returns ``(status, out)``,
+    out uint32 [C, ld] with column j of the receive rows in out[j, :rows].
+    ``ld`` defaults to ``rows`` rounded up to a multiple of 4.  A new ``out``
+    is filled with 0xA5A5A5A5 so words the oracle leaves alone stay visible."""
+    lib = lib or load()
+    sf = _as(sf_words, np.uint32)
+    dst = _as(dst_slot, np.int32)
+    off = _as(expert_offset, np.int32)
+    cnt = _as(expert_count, np.int32)
+    N, C = sf.shape
+    K = dst.shape[1] if dst.ndim == 2 else (dst.size // max(N, 1) if N else 1)
+    ld = (rows + 3) // 4 * 4 if ld is None else ld
+    out = np.full((C, max(ld, 0)), 0xA5A5A5A5, np.uint32)
+    st = lib.oracle_permute_sf_col_major(N, K, _ptr(dst), _ptr(sf), C, cnt.shape[0], _ptr(off), _ptr(cnt),
+                                         _ptr(out), ld, rows, 1 if zero_pad else 0)
+    return int(st), out
 
 
 def f32_to_bf16(a, lib: ctypes.CDLL | None = None) -> np.ndarray:

@@ -8,6 +8,8 @@
  * calls it.  Every step follows the page
  *   "07 DeepEP Counting Sort / Bucketization 深度校验：博客第一性原理 vs 源码实现"
  *   (DeepEP v2 source notes), cited below as [CS] with its section numbers.
+ * The column-major scale-factor layout follows an option named on the page
+ * "00 DeepEP Engram Architecture Deep-Dive", cited as [EA].
  *
  * Notation: N tokens, K top-k slots per token, E experts, R logical ranks,
  * L = E / R experts per rank, A the expert alignment.  topk_idx[t*K + k] is
@@ -233,6 +235,46 @@ int oracle_permute(int64_t N, int32_t K, const int32_t *dst_slot,
         memset(recv_x + i * row_bytes, 0, (size_t)row_bytes);
         if (sf) memset(recv_sf + i * sf_row_bytes, 0, (size_t)sf_row_bytes);
       }
+    }
+  }
+  return ORACLE_OK;
+}
+
+/*
+ * oracle_permute_sf_col_major -- the scale factors of the expand-mode receive
+ * buffer stored column-major with a TMA-aligned leading dimension: the fetch
+ * option use_tma_aligned_col_major_sf of the page "00 DeepEP Engram
+ * Architecture Deep-Dive" (§1.1 Python API, §1.2 C++ runtime), cited here as
+ * [EA].  [EA] names the option and defines nothing.  Reading taken: the
+ * [rows, C] matrix of 4-byte scale words is stored one column after another,
+ * column j at out + j*ld, and ld (the leading dimension) is a row count that
+ * is a multiple of 4, so that every column starts on a 16-byte boundary as a
+ * TMA global stride must.  Rows move as in oracle_permute ([CS] §6.4, §8.2):
+ *   out[j*ld + dst_slot[t*K+k]] = sf[t*C + j]   for every valid pair, all j;
+ * with zero_pad, rows [expert_offset[e] + expert_count[e], expert_offset[e+1])
+ * are 0 in every column ([CS] §7.3).  Nothing else is written.  ld must be at
+ * least `rows` (the rows the layout uses) and a multiple of 4.
+ */
+int oracle_permute_sf_col_major(int64_t N, int32_t K, const int32_t *dst_slot,
+                                const uint32_t *sf, int64_t C, int32_t E,
+                                const int32_t *expert_offset,
+                                const int32_t *expert_count, uint32_t *out,
+                                int64_t ld, int64_t rows, int32_t zero_pad) {
+  if (N < 0 || K < 1 || C < 0 || ld < rows || ld % 4 != 0) return ORACLE_BAD_ARG;
+  for (int64_t t = 0; t < N; ++t) {
+    for (int32_t k = 0; k < K; ++k) {
+      int64_t s = dst_slot[t * K + k];
+      if (s < 0) continue;
+      if (s >= rows) return ORACLE_CAPACITY;
+      for (int64_t j = 0; j < C; ++j) out[j * ld + s] = sf[t * C + j];
+    }
+  }
+  if (zero_pad) {
+    for (int32_t e = 0; e < E; ++e) {
+      int64_t gap_begin = (int64_t)expert_offset[e] + expert_count[e];
+      int64_t gap_end = expert_offset[e + 1];
+      for (int64_t i = gap_begin; i < gap_end && i < rows; ++i)
+        for (int64_t j = 0; j < C; ++j) out[j * ld + i] = 0;
     }
   }
   return ORACLE_OK;

@@ -30,6 +30,11 @@ What pins what (page: "07 DeepEP Counting Sort / Bucketization", sections):
   rank_sort      -- the non-expand (rank-contiguous) rows as a library sort of the
                     distinct (token, rank) pairs; master lane = highest k (§6.2);
                     also part of handworked and bruteforce.
+  sf_col_major   -- column-major scale factors (option named on the page "00
+                    DeepEP Engram Architecture Deep-Dive", §1.1-§1.2): columns
+                    derived by hand (golden file), a gather through src_idx,
+                    the transpose of the row-major scatter, untouched words past
+                    the rows, and the leading-dimension rule.
 """
 from __future__ import annotations
 
@@ -570,11 +575,57 @@ def check_errors(lib):
     assert rr["status"] == oracle.CAPACITY and rr["total_rows"] == 3
 
 
+def check_sf_col_major(lib, seed=19):
+    g = json.load(open(os.path.join(GOLDEN, "handworked_n4_k2_e4_r2_a2.json")))
+    sfw = np.array(g["sf_words"], np.uint32)
+    st, out = oracle.permute_sf_col_major(sfw, g["dst_slot"], g["expert_offset"], g["expert_count"],
+                                          g["total_rows"], lib=lib)
+    assert st == oracle.OK and out.shape == (3, 8)
+    np.testing.assert_array_equal(out, g["sf_col_major"])
+    # a wider leading dimension: words past the rows are not written
+    st, out = oracle.permute_sf_col_major(sfw, g["dst_slot"], g["expert_offset"], g["expert_count"],
+                                          g["total_rows"], ld=12, lib=lib)
+    assert st == oracle.OK
+    np.testing.assert_array_equal(out[:, :8], g["sf_col_major"])
+    assert np.all(out[:, 8:] == 0xA5A5A5A5)
+    # leading dimension must cover the rows and be a multiple of 4 words (16 bytes)
+    for ld in (6, 10):
+        st, _ = oracle.permute_sf_col_major(sfw, g["dst_slot"], g["expert_offset"], g["expert_count"],
+                                            g["total_rows"], ld=ld, lib=lib)
+        assert st == oracle.BAD_ARG, ld
+
+    rng = np.random.default_rng(seed)
+    N, K, E, R, A, C = 300, 8, 32, 4, 16, 7
+    idx = random_idx(rng, N, K, E, 0.15)
+    r = oracle.layout(idx, E, R, A, lib=lib)
+    rows = r["total_rows"]
+    sf = rng.integers(0, 2**32, size=(N, C), dtype=np.uint32)
+    src = r["src_idx"]
+    real = src >= 0
+    ld = (rows + 3) // 4 * 4 + 4
+    st, out = oracle.permute_sf_col_major(sf, r["dst_slot"], r["expert_offset"], r["expert_count"], rows,
+                                          ld=ld, lib=lib)
+    assert st == oracle.OK
+    # gather formulation: column j of row i is word j of token src_idx[i]
+    np.testing.assert_array_equal(out[:, :rows][:, real], sf[src[real]].T)
+    assert np.all(out[:, :rows][:, ~real] == 0)
+    assert np.all(out[:, rows:] == 0xA5A5A5A5)
+    # the transpose of the row-major scatter of the same words
+    _, _, recv_sf = oracle.permute(np.zeros((N, 16), np.uint8), r["dst_slot"], r["expert_offset"],
+                                   r["expert_count"], rows, sf_bytes=sf.view(np.uint8).reshape(N, 4 * C), lib=lib)
+    np.testing.assert_array_equal(out[:, :rows], recv_sf.view(np.uint32).reshape(rows, C).T)
+    # without zero padding the gap rows keep what was there
+    st, out2 = oracle.permute_sf_col_major(sf, r["dst_slot"], r["expert_offset"], r["expert_count"], rows,
+                                           zero_pad=False, lib=lib)
+    np.testing.assert_array_equal(out2[:, :rows][:, real], sf[src[real]].T)
+    assert np.all(out2[:, :rows][:, ~real] == 0xA5A5A5A5)
+
+
 ALL_CHECKS = [
     check_handworked, check_padding_example, check_sort_formulation, check_rank_sort_formulation,
     check_invariants,
     check_bruteforce, check_permute, check_combine_closed_form, check_combine_bound,
-    check_combine_exact, check_roundtrip_direct, check_bf16, check_errors,
+    check_combine_exact, check_roundtrip_direct, check_bf16, check_errors, check_sf_col_major,
 ]
 
 

@@ -51,6 +51,12 @@ MUTATIONS = [
      "count[r] += 1;"),
     ("rank_rows_no_dedup", "if (taken) continue;", "(void)taken;"),
     ("rank_block_start_inclusive", "cursor[r] = run; run += count[r];", "run += count[r]; cursor[r] = run - 1;"),
+    ("sf_col_major_stored_row_major", "for (int64_t j = 0; j < C; ++j) out[j * ld + s] = sf[t * C + j];",
+     "for (int64_t j = 0; j < C; ++j) out[s * C + j] = sf[t * C + j];"),
+    ("sf_col_major_columns_reversed", "for (int64_t j = 0; j < C; ++j) out[j * ld + s] = sf[t * C + j];",
+     "for (int64_t j = 0; j < C; ++j) out[j * ld + s] = sf[t * C + (C - 1 - j)];"),
+    ("sf_col_major_no_zero_pad", "for (int64_t j = 0; j < C; ++j) out[j * ld + i] = 0;", "(void)0;"),
+    ("sf_col_major_ld_not_checked", "ld < rows || ld % 4 != 0", "ld < 0"),
 ]
 
 
