@@ -217,20 +217,25 @@ class OracleRunner:
 
 
 # ------------------------------------------------------------ native run
-def algorithmic_bytes(w: wl.Workload, lay) -> dict:
-    """Bytes each kernel must move, from the layout of this batch."""
+def algorithmic_bytes(w: wl.Workload, lay, sf_col_major: bool = False) -> dict:
+    """Bytes each kernel must move, from the layout of this batch.  With
+    ``sf_col_major`` the permute moves the rows only and the scale factors
+    go column-major in their own kernel (reads each routed token's scale
+    row, writes every receive row's words, reads the inverse map)."""
     N, K, E = w.num_tokens, w.topk, w.num_experts
     dst = lay.dst_slot[: N * K].view(N, K)
     valid = dst >= 0
     P = int(valid.sum().item())
     n_tok = int(valid.any(dim=1).sum().item())
     rows = int(lay.total_rows.item())
-    rb = w.row_bytes + w.sf_row_bytes
+    rb = w.row_bytes + (0 if sf_col_major else w.sf_row_bytes)
     permute = n_tok * rb + P * rb + (rows - P) * rb + N * K * 4 + 2 * (E + 1) * 4
+    sf_cm = n_tok * w.sf_row_bytes + rows * w.sf_row_bytes + rows * 4 if sf_col_major else 0
     combine = P * w.hidden * 2 + N * K * 8 + N * w.hidden * 2 if w.row_dtype == "bf16" else 0
     count = N * K * 8
     scan = N * K * 8 + N * K * 4 + rows * 4
-    return {"permute": permute, "combine": combine, "count": count, "scan": scan, "P": P, "rows": rows,
+    return {"permute": permute, "combine": combine, "count": count, "scan": scan, "sf_col_major": sf_cm,
+            "P": P, "rows": rows,
             "tokens_routed": n_tok}
 
 
@@ -286,6 +291,10 @@ def run_native(args, rank, world, local):
     lay = binding.Layout(w, cap, device=dev)
     recv = torch.empty((cap, H), dtype=x_d.dtype, device=dev)
     recv_sf = torch.empty((cap, sf_d.shape[1]), dtype=sf_d.dtype, device=dev) if sf_d is not None else None
+    sf_cm = args.sf_col_major and sf_d is not None
+    # Column-major scale factors: the permute moves rows only, then its own kernel.
+    recv_sf_cm = binding.new_sf_col_major(sf_d.shape[1], cap, device=dev) if sf_cm else None
+    perm_sf, perm_recv_sf = (None, None) if sf_cm else (sf_d, recv_sf)
     do_combine = w.row_dtype == "bf16"
     out = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
     # The combine's input: the round-trip stand-in expert applied once to a
@@ -310,13 +319,16 @@ def run_native(args, rank, world, local):
         ev[0].record(stream)
         lay.build(idx_d)
         ev[1].record(stream)
-        lay.permute(x_d, recv, sf_d, recv_sf)
+        lay.permute(x_d, recv, perm_sf, perm_recv_sf)
         ev[2].record(stream)
+        if sf_cm:
+            lay.permute_sf_col_major(sf_d, recv_sf_cm)
+        ev[3].record(stream)
         if do_combine:
             lay.combine(eo, wt_d, out)
-        ev[3].record(stream)
+        ev[4].record(stream)
 
-    new_events = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    new_events = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(5)]
     for _ in range(args.warmup):
         flush_l2()
         step(new_events())
@@ -343,13 +355,13 @@ def run_native(args, rank, world, local):
     err = lay.error()
     assert err == 0, f"device error {err} in the timed region"
 
-    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(3)] for e in evs])   # ms
+    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in evs])   # ms
     step_ms = per.sum(axis=1)
     ms_per_step = reduce_max(float(step_ms.mean()), world, dev)
-    kern_ms = per.mean(axis=0)     # layout (count + scan + rank), permute, combine
-    ab = algorithmic_bytes(w, lay)
+    kern_ms = per.mean(axis=0)     # layout (count + scan + rank), permute, column-major scales, combine
+    ab = algorithmic_bytes(w, lay, sf_cm)
     value = world * N / (ms_per_step / 1e3)
-    dispatch_ms = float(kern_ms[:2].sum())
+    dispatch_ms = float(kern_ms[:3].sum())
 
     # End to end through the public API with host buffers: pinned ids, rows
     # and weights in, the combined tokens back.  moe_dispatch_from_host and
@@ -402,9 +414,12 @@ def run_native(args, rank, world, local):
         "roofline": {"kernel": "permute_dyn_kernel", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "peak_source": peaks["source"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "traffic": traffic, "algorithmic_bytes_per_launch": ab["permute"]},
-        "kernels_ms": {"layout": kern_ms[0], "permute": kern_ms[1], "combine": kern_ms[2] if do_combine else None},
+        "kernels_ms": {"layout": kern_ms[0], "permute": kern_ms[1],
+                       "sf_col_major": kern_ms[2] if sf_cm else None,
+                       "combine": kern_ms[3] if do_combine else None},
         "kernels_gbs": {"permute": ab["permute"] / permute_s / 1e9,
-                        "combine": (ab["combine"] / (kern_ms[2] / 1e3) / 1e9) if do_combine else None},
+                        "sf_col_major": (ab["sf_col_major"] / (kern_ms[2] / 1e3) / 1e9) if sf_cm else None,
+                        "combine": (ab["combine"] / (kern_ms[3] / 1e3) / 1e9) if do_combine else None},
         "dispatch_tokens_per_s": world * N / (dispatch_ms / 1e3),
         "layout": {"valid_pairs": ab["P"], "rows": ab["rows"], "tokens_routed": ab["tokens_routed"]},
         "e2e": {"value": world * N / (e2e_step_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -414,6 +429,9 @@ def run_native(args, rank, world, local):
         "wall_s_timed_region": t_wall,
         "clocks": sampler.summary() if sampler else None,
     }
+    if sf_d is not None:
+        line["config"]["sf_layout"] = ("column-major, ld = capacity rounded up to 4 words (e2e leg: row-major)"
+                                       if sf_cm else "row-major, moved by the permute")
     if world == 1 and not args.no_cpu_baseline:
         runner = OracleRunner(w, inp)
         tps, passes = runner.time_passes(args.cpu_seconds, args.cpu_max_passes)
@@ -477,6 +495,8 @@ def parse_args(argv=None):
     ap.add_argument("--ref-seconds", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--sf-col-major", action="store_true",
+                    help="fp8 workloads: scale factors column-major (TMA-aligned) by their own kernel")
     ap.add_argument("--layout-only", action="store_true",
                     help="time only the layout step (count, scan, maps) on the chosen workload")
     return ap.parse_args(argv)

@@ -16,7 +16,7 @@ import importlib
 _BINDING_NAMES = (
     "Layout", "LayoutDesc", "LayoutError", "workspace_bytes", "new_workspace", "layout_count", "layout_scan",
     "layout_build", "layout_rank_rows", "dispatch_permute_ranks", "dispatch_from_host", "combine_to_host",
-    "accumulate_stats",
+    "accumulate_stats", "dispatch_sf_col_major", "new_sf_col_major", "sf_col_major_ld",
     "dispatch_permute", "combine_unpermute", "get_error", "kernel_launches", "strerror",
     "library_path", "load_library", "dispatch", "ERROR_NAMES",
 )

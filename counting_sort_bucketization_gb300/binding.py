@@ -82,6 +82,7 @@ def load_library() -> ctypes.CDLL:
         lib.moe_combine_to_host.argtypes = [dp, p, i64, i64, p, p, p, p, p, sz, i64, p, p]
         lib.moe_dispatch_permute_ranks.argtypes = [dp, p, i64, p, i64, p, p, p, p, i64, p, sz, p]
         lib.moe_combine_unpermute.argtypes = [dp, p, i64, i64, p, p, p, p, sz, p]
+        lib.moe_dispatch_sf_col_major.argtypes = [dp, p, i64, p, p, p, i64, i64, ctypes.c_int, p, sz, p]
         lib.moe_layout_get_error.argtypes = [p, ctypes.POINTER(i32), p]
         lib.moe_strerror.argtypes = [ctypes.c_int]
         lib.moe_strerror.restype = ctypes.c_char_p
@@ -91,7 +92,8 @@ def load_library() -> ctypes.CDLL:
                      "moe_layout_build_i32",
                      "moe_layout_rank_rows", "moe_dispatch_permute_ranks", "moe_dispatch_from_host",
                      "moe_combine_to_host", "moe_layout_accumulate_stats",
-                     "moe_dispatch_permute", "moe_combine_unpermute", "moe_layout_get_error"):
+                     "moe_dispatch_permute", "moe_combine_unpermute", "moe_layout_get_error",
+                     "moe_dispatch_sf_col_major"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -248,6 +250,32 @@ def dispatch_permute_ranks(desc, x, rank_slot, rank_psum, recv, workspace, sf=No
     _check(st, "moe_dispatch_permute_ranks")
 
 
+def sf_col_major_ld(capacity_rows: int) -> int:
+    """Leading dimension of a column-major scale buffer: rows rounded up to 4 words (16 bytes)."""
+    return (int(capacity_rows) + 3) // 4 * 4
+
+
+def new_sf_col_major(cols: int, capacity_rows: int, dtype=torch.float32, device="cuda") -> torch.Tensor:
+    """Storage [cols, ld] for column-major scale factors; ``.t()[:capacity_rows]`` is the [rows, cols] view."""
+    return torch.empty((int(cols), sf_col_major_ld(capacity_rows)), dtype=dtype, device=device)
+
+
+def dispatch_sf_col_major(desc, sf, src, total_rows, recv_sf_cm, capacity_rows, workspace, zero_pad=True,
+                          stream=None) -> None:
+    """recv_sf_cm[j, i] = sf[src[i], j] for the receive rows i (column-major, ld = recv_sf_cm.shape[1])."""
+    N = int(desc.num_tokens)
+    if sf.element_size() != 4 or recv_sf_cm.element_size() != 4:
+        raise ValueError("sf and recv_sf_cm must have 4-byte elements")
+    if sf.dim() != 2 or sf.shape[0] != N or recv_sf_cm.dim() != 2 or recv_sf_cm.shape[0] != sf.shape[1]:
+        raise ValueError("sf must be [N, C] and recv_sf_cm [C, ld]")
+    st = load_library().moe_dispatch_sf_col_major(
+        ctypes.byref(_desc(desc)), _dev(sf, "sf"), sf.shape[1], _dev(src, "src", torch.int32, capacity_rows),
+        _dev(total_rows, "total_rows", torch.int32, 1), _dev(recv_sf_cm, "recv_sf_cm"), recv_sf_cm.shape[1],
+        int(capacity_rows), 1 if zero_pad else 0, _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+        _stream(stream))
+    _check(st, "moe_dispatch_sf_col_major")
+
+
 def combine_unpermute(desc, expert_out, dst_slot, weights, out, workspace, stream=None) -> None:
     """out[t] = bf16(sum_k w[t,k] * expert_out[dst_slot[t,k]]) with an fp32 fma chain."""
     N, K = int(desc.num_tokens), int(desc.topk)
@@ -373,6 +401,11 @@ class Layout:
         dispatch_permute(self.desc, x, self.dst_slot, self.expert_offset, self.expert_count, recv_x,
                          self.workspace, sf, recv_sf, zero_pad, stream)
 
+    def permute_sf_col_major(self, sf, recv_sf_cm, zero_pad=True, stream=None):
+        """Scale factors of the expand layout, column-major into ``recv_sf_cm`` [C, ld]."""
+        dispatch_sf_col_major(self.desc, sf, self.src_idx, self.total_rows, recv_sf_cm, self.capacity,
+                              self.workspace, zero_pad, stream)
+
     def rank_rows(self, topk_idx, capacity_rows=None, stream=None):
         """Non-expand slot map after ``build``: sets ``rank_slot`` [N*K] and ``rank_src`` [capacity]."""
         N, K, R = int(self.desc.num_tokens), int(self.desc.topk), int(self.desc.num_ranks)
@@ -387,6 +420,12 @@ class Layout:
     def permute_ranks(self, x, recv, sf=None, recv_sf=None, stream=None):
         dispatch_permute_ranks(self.desc, x, self.rank_slot, self.rank_psum, recv, self.workspace, sf, recv_sf,
                                stream)
+
+    def permute_sf_col_major_ranks(self, sf, recv_sf_cm, stream=None):
+        """Scale factors of the non-expand layout (after ``rank_rows``), column-major."""
+        R = int(self.desc.num_ranks)
+        dispatch_sf_col_major(self.desc, sf, self.rank_src, self.rank_psum[R - 1:], recv_sf_cm,
+                              self.rank_src.numel(), self.workspace, False, stream)
 
     def combine(self, expert_out, weights, out, stream=None):
         combine_unpermute(self.desc, expert_out, self.dst_slot, weights, out, self.workspace, stream)

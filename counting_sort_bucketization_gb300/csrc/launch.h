@@ -79,6 +79,21 @@ struct CombineArgs {
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);
 
+struct SfColMajorArgs {
+  const uint32_t* sf;          // [num_tokens, cols] 4-byte scale words
+  int64_t cols;
+  const int32_t* src;          // token of each receive row; -1 = gap row
+  const int32_t* total_rows;   // rows in use (checked against capacity)
+  uint32_t* out;               // column j at out + j * ld
+  int64_t ld;
+  int64_t capacity;
+  int64_t num_tokens;
+  int zero_pad;
+  int* err;
+};
+
+cudaError_t launch_sf_col_major(const SfColMajorArgs& a, cudaStream_t stream);
+
 // Streaming multiprocessors of the current device (cached per device).
 int device_sm_count();
 

@@ -236,6 +236,31 @@ int moe_dispatch_permute_ranks(const moe_layout_desc* desc, const void* x, int64
   return cuda_status(launch_permute(a, static_cast<cudaStream_t>(stream)));
 }
 
+int moe_dispatch_sf_col_major(const moe_layout_desc* desc, const void* sf, int64_t sf_cols, const int32_t* src,
+                              const int32_t* total_rows, void* recv_sf_cm, int64_t ld, int64_t capacity_rows,
+                              int zero_pad, void* workspace, size_t workspace_bytes, void* stream) {
+  if (int st = check_desc(desc)) return st;
+  WorkspaceLayout w;
+  if (int st = check_workspace(desc, workspace, workspace_bytes, &w)) return st;
+  if (sf_cols <= 0 || capacity_rows < 0 || ld < capacity_rows || ld % 4 != 0 || total_rows == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if ((desc->num_tokens > 0 && sf == nullptr) || (capacity_rows > 0 && (src == nullptr || recv_sf_cm == nullptr)))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(sf, 4) || !aligned(recv_sf_cm, 16)) return MOE_ERR_INVALID_ARG;
+  SfColMajorArgs a{};
+  a.sf = static_cast<const uint32_t*>(sf);
+  a.cols = sf_cols;
+  a.src = src;
+  a.total_rows = total_rows;
+  a.out = static_cast<uint32_t*>(recv_sf_cm);
+  a.ld = ld;
+  a.capacity = capacity_rows;
+  a.num_tokens = desc->num_tokens;
+  a.zero_pad = zero_pad != 0;
+  a.err = at<int>(workspace, w.err_off);
+  return cuda_status(launch_sf_col_major(a, static_cast<cudaStream_t>(stream)));
+}
+
 int moe_combine_unpermute(const moe_layout_desc* desc, const void* expert_out, int64_t expert_out_rows,
                           int64_t hidden, const int32_t* dst_slot, const float* weights, void* out,
                           void* workspace, size_t workspace_bytes, void* stream) {

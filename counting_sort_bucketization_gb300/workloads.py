@@ -133,6 +133,13 @@ def draw_x(w: Workload, seed: int) -> tuple[torch.Tensor, torch.Tensor | None]:
     return q.view(N, H).to(torch.float8_e4m3fn).contiguous(), sf.to(torch.float32).contiguous()
 
 
+def draw_sf_words(num_tokens: int, cols: int, seed: int) -> torch.Tensor:
+    """int32 [N, cols]: arbitrary 32-bit scale words (any bit pattern: the layouts move them verbatim)."""
+    g = _gen(seed, 6)
+    return torch.randint(-(2 ** 31), 2 ** 31, (num_tokens, cols), dtype=torch.int64, generator=g).to(
+        torch.int32).contiguous()
+
+
 def draw_weights(w: Workload, seed: int) -> torch.Tensor:
     """fp32 [N, K]: softmax over the K slots of N(0,1) logits (masked slots keep their weight; combine skips them)."""
     g = _gen(seed, 5)

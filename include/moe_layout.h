@@ -203,6 +203,36 @@ MOE_API int moe_dispatch_permute_ranks(const moe_layout_desc* desc, const void* 
                                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Scale factors of a receive buffer in column-major, TMA-aligned form.  The
+ * page "00 DeepEP Engram Architecture Deep-Dive" (§1.1 Python API, §1.2 C++
+ * runtime) names the option use_tma_aligned_col_major_sf and does not define
+ * it.  Reading taken: the [rows, sf_cols] matrix of 4-byte scale words (fp32
+ * scales, or packed exponents: moved verbatim) is stored column after
+ * column, column j at recv_sf_cm + j*ld words, and ld is a multiple of 4 so
+ * that every column starts on a 16-byte boundary (a TMA global stride must
+ * be a multiple of 16 bytes).  Rows follow the layout's inverse map:
+ *   recv_sf_cm[j*ld + i] = sf[src[i]*sf_cols + j]   for i < rows, src[i] >= 0;
+ * rows with src[i] = -1 (the alignment gaps of the expand layout, [CS] §7.3)
+ * are zero in every column when zero_pad != 0 and are not written
+ * otherwise; rows >= rows are never written.
+ *   sf [N, sf_cols] 4-byte words, 4-byte aligned; sf_cols >= 1;
+ *   src: src_idx of moe_layout_build (expand layout) or rank_src of
+ *        moe_layout_rank_rows (non-expand layout), entries in [-1, N);
+ *   total_rows: device int32[1] holding rows: the total_rows output of
+ *        moe_layout_build, or rank_psum + R - 1;
+ *   recv_sf_cm [sf_cols, ld] words, 16-byte aligned, ld >= capacity_rows,
+ *        ld a multiple of 4.
+ * rows > capacity_rows records MOE_ERR_CAPACITY and nothing is written; a
+ * src entry outside [-1, N) is skipped and records MOE_ERR_INVALID_ARG.
+ * Independent of moe_dispatch_permute: call it instead of passing sf there,
+ * on the same stream, after the layout.
+ */
+MOE_API int moe_dispatch_sf_col_major(const moe_layout_desc* desc, const void* sf, int64_t sf_cols,
+                                      const int32_t* src, const int32_t* total_rows, void* recv_sf_cm,
+                                      int64_t ld, int64_t capacity_rows, int zero_pad, void* workspace,
+                                      size_t workspace_bytes, void* stream);
+
+/*
  * Combine: the inverse of the dispatch.  The pages keep the slot map for it
  * ([CS] §6.2) but print no arithmetic; this is the plain definition
  *   out[t, h] = bf16( sum over k = 0..K-1 with dst_slot[t*K+k] >= 0 of

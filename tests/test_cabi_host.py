@@ -86,6 +86,15 @@ def test_host_checks_reject_before_launch(lib):
     # combine: hidden not a multiple of 8, null weights
     assert lib.moe_combine_unpermute(d, fake, 10, 12, fake, fake, fake, fake, n.value, None) == 1
     assert lib.moe_combine_unpermute(d, fake, 10, 16, fake, None, fake, fake, n.value, None) == 1
+    # column-major scale factors: ld not a multiple of 4 or below capacity, no columns,
+    # output not 16-byte aligned, missing total or map
+    sfa = lambda C, src, tot, out, ld: (d, fake, C, src, tot, out, ld, 100, 1, fake, n.value, None)
+    assert lib.moe_dispatch_sf_col_major(*sfa(56, fake, fake, fake, 102)) == 1
+    assert lib.moe_dispatch_sf_col_major(*sfa(56, fake, fake, fake, 96)) == 1
+    assert lib.moe_dispatch_sf_col_major(*sfa(0, fake, fake, fake, 100)) == 1
+    assert lib.moe_dispatch_sf_col_major(*sfa(56, fake, fake, ctypes.c_void_p((1 << 20) + 4), 100)) == 1
+    assert lib.moe_dispatch_sf_col_major(*sfa(56, fake, None, fake, 100)) == 1
+    assert lib.moe_dispatch_sf_col_major(*sfa(56, None, fake, fake, 100)) == 1
     assert lib.moe_layout_get_error(None, None, None) == 1
 
 
