@@ -21,8 +21,8 @@
  *  - Return value: MOE_OK, or an error found on the host before anything was
  *    launched (MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED), or MOE_ERR_CUDA if a
  *    launch failed.  Errors found by the kernels (bad expert id, capacity,
- *    timeout) are recorded in the workspace's sticky error word and read
- *    with moe_layout_get_error().
+ *    timeout, an inverse-map entry out of range) are recorded in the
+ *    workspace's sticky error word and read with moe_layout_get_error().
  *  - Notation: N tokens, K top-k slots, E experts, R logical ranks,
  *    L = E / R experts per rank, A alignment.  Logical rank r owns experts
  *    [r*L, (r+1)*L); ranks are partitions of one GPU buffer, not devices.
@@ -56,7 +56,8 @@ extern "C" {
 /* Status codes.  0 is success. */
 enum moe_status {
   MOE_OK = 0,
-  MOE_ERR_INVALID_ARG = 1,   /* host check failed: null pointer, bad size or alignment  */
+  MOE_ERR_INVALID_ARG = 1,   /* host check failed: null pointer, bad size or alignment;
+                                device (moe_dispatch_sf_col_major): map entry out of range */
   MOE_ERR_CUDA = 2,          /* a CUDA launch or copy failed                           */
   MOE_ERR_BAD_EXPERT_ID = 3, /* device: some topk_idx entry was >= E                   */
   MOE_ERR_CAPACITY = 4,      /* device: the layout needs more rows than capacity_rows  */

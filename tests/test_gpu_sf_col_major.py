@@ -95,8 +95,40 @@ def test_edge(w, cols):
     np.testing.assert_array_equal(got, want)
 
 
-def test_gap_rows_left_alone_without_zero_pad():
-    err, got, want, _, _ = expand_case(wl.WORKLOADS["skewed"], wl.SEEDS["skewed"], cols=9, zero_pad=False)
+@pytest.mark.parametrize("name", ["tiny", "decode"])
+def test_rows_wider_than_one_pass(name):
+    # 200 words a row: 4 passes of 64 columns through the tile, the last one partial
+    err, got, want, _, _ = expand_case(wl.WORKLOADS[name], wl.SEEDS[name], cols=200)
+    assert err == 0
+    np.testing.assert_array_equal(got, want)
+
+
+def test_scale_rows_not_16_byte_aligned():
+    # a base 4 bytes past a 16-byte boundary: single-word loads, same result
+    w = wl.WORKLOADS["decode"]
+    seed = wl.SEEDS["decode"]
+    inp = wl.make(w, seed)
+    N, C = w.num_tokens, 56
+    sf = wl.draw_sf_words(N, C, seed)
+    flat = torch.empty(N * C + 4, dtype=torch.int32, device=DEV)
+    sf_d = flat[1: 1 + N * C].view(N, C)
+    sf_d.copy_(sf.to(DEV))
+    assert sf_d.data_ptr() % 16 == 4
+    ref = oracle.layout(inp["topk_idx"].numpy(), w.num_experts, w.num_ranks, w.alignment)
+    cap = wl.worst_case_rows(w)
+    lay = binding.Layout(w, cap, device=DEV).build(inp["topk_idx"].to(DEV))
+    ld = binding.sf_col_major_ld(cap)
+    out = sentinel_buffer(C, ld)
+    lay.permute_sf_col_major(sf_d, out)
+    assert lay.error() == 0
+    _, want = oracle.permute_sf_col_major(words(sf), ref["dst_slot"], ref["expert_offset"], ref["expert_count"],
+                                          ref["total_rows"], ld=ld)
+    np.testing.assert_array_equal(words(out), want)
+
+
+@pytest.mark.parametrize("cols", [9, 56])
+def test_gap_rows_left_alone_without_zero_pad(cols):
+    err, got, want, _, _ = expand_case(wl.WORKLOADS["skewed"], wl.SEEDS["skewed"], cols=cols, zero_pad=False)
     assert err == 0
     np.testing.assert_array_equal(got, want)
 
