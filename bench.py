@@ -364,39 +364,45 @@ def run_native(args, rank, world, local):
     dispatch_ms = float(kern_ms[:3].sum())
 
     # End to end through the public API with host buffers: pinned ids, rows
-    # and weights in, the combined tokens back.  moe_dispatch_from_host and
-    # moe_combine_to_host overlap the copies with the kernels in chunks; the
-    # copies are inside the timed region.
+    # and weights in, the combined tokens back (dispatch-only workloads: the
+    # receive rows back).  moe_dispatch_from_host and moe_combine_to_host
+    # overlap the copies with the kernels in chunks, and HostPipeline keeps
+    # `--e2e-lanes` batches in flight so one batch's copy back overlaps the
+    # next one's copy in.  Every copy is inside the timed region; each
+    # step's working set (rows, receive buffer) is larger than L2.
     idx_h = inp["topk_idx"].pin_memory()
     x_h = inp["x"].pin_memory()
     sf_h = inp["sf"].pin_memory() if inp["sf"] is not None else None
     wt_h = inp["weights"].pin_memory()
-    out_h = torch.empty((N, H), dtype=torch.bfloat16).pin_memory()
-    recv_h = None if do_combine else torch.empty((cap, H), dtype=x_d.dtype).pin_memory()
+    out_shape, out_dtype = ((N, H), torch.bfloat16) if do_combine else ((cap, H), x_d.dtype)
+    lanes = max(1, args.e2e_lanes)
+    outs_h = [torch.empty(out_shape, dtype=out_dtype).pin_memory() for _ in range(lanes)]
     h2d = idx_h.numel() * 8 + x_h.numel() * x_h.element_size() + wt_h.numel() * 4 + \
         (sf_h.numel() * 4 if sf_h is not None else 0)
-    d2h = out_h.numel() * 2 if do_combine else recv_h.numel() * recv_h.element_size()
+    d2h = outs_h[0].numel() * outs_h[0].element_size()
     chunk = -(-N // max(1, args.e2e_chunks))
-    copy_stream = torch.cuda.Stream(dev)
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
-    e2e_ms = []
-    for i in range(e2e_steps + 2):
-        flush_l2()
+    expert = (lambda lay_, recv_, recv_sf_: eo) if do_combine else None
+
+    def e2e_ms_per_step(n_lanes):
+        pipe = binding.HostPipeline(w, cap, H, x_dtype=x_d.dtype, sf_cols=sf_d.shape[1] if sf_d is not None else 0,
+                                    lanes=n_lanes, chunk_tokens=chunk, device=dev)
+        for i in range(2 * n_lanes):
+            pipe.submit(idx_h, x_h, wt_h, outs_h[i % n_lanes], expert, sf_h)
+        pipe.join(stream)
+        torch.cuda.synchronize(dev)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        binding.dispatch_from_host(lay, idx_h, x_h, idx_d, x_d, recv, weights_host=wt_h, weights=wt_d,
-                                   sf_host=sf_h, sf=sf_d, recv_sf=recv_sf, chunk_tokens=chunk,
-                                   copy_stream=copy_stream)
-        if do_combine:
-            binding.combine_to_host(lay, eo, wt_d, out, out_h, chunk_tokens=chunk, copy_stream=copy_stream)
-        else:
-            recv_h.copy_(recv, non_blocking=True)
+        for i in range(e2e_steps):
+            pipe.submit(idx_h, x_h, wt_h, outs_h[i % n_lanes], expert, sf_h)
+        pipe.join(stream)
         b.record(stream)
-        if i >= 2:
-            e2e_ms.append((a, b))
-    torch.cuda.synchronize(dev)
-    e2e_step_ms = reduce_max(float(np.mean([a.elapsed_time(b) for a, b in e2e_ms])), world, dev)
-    assert lay.error() == 0, "device error in the end-to-end steps"
+        torch.cuda.synchronize(dev)
+        assert pipe.errors() == [0] * n_lanes, "device error in the end-to-end steps"
+        return a.elapsed_time(b) / e2e_steps
+
+    e2e_step_ms = reduce_max(e2e_ms_per_step(lanes), world, dev)
+    e2e_one_ms = reduce_max(e2e_ms_per_step(1), world, dev) if lanes > 1 else e2e_step_ms
 
     if rank != 0:
         return
@@ -424,7 +430,9 @@ def run_native(args, rank, world, local):
         "layout": {"valid_pairs": ab["P"], "rows": ab["rows"], "tokens_routed": ab["tokens_routed"]},
         "e2e": {"value": world * N / (e2e_step_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps, "chunks": args.e2e_chunks,
-                "api": "moe_dispatch_from_host + moe_combine_to_host"},
+                "batches_in_flight": lanes, "value_one_batch_in_flight": world * N / (e2e_one_ms / 1e3),
+                "api": "HostPipeline: moe_dispatch_from_host + moe_combine_to_host" if do_combine
+                else "HostPipeline: moe_dispatch_from_host + receive rows copied back"},
         "gpu_launches": launches,
         "wall_s_timed_region": t_wall,
         "clocks": sampler.summary() if sampler else None,
@@ -490,6 +498,7 @@ def parse_args(argv=None):
     ap.add_argument("--workload", choices=list(wl.WORKLOADS), default="decode")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--e2e-chunks", type=int, default=4, help="token chunks the host copies are split into")
+    ap.add_argument("--e2e-lanes", type=int, default=3, help="batches in flight in the end-to-end leg")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-max-passes", type=int, default=20)
     ap.add_argument("--ref-seconds", type=float, default=90.0)

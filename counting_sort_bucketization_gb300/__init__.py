@@ -18,7 +18,7 @@ _BINDING_NAMES = (
     "layout_build", "layout_rank_rows", "dispatch_permute_ranks", "dispatch_from_host", "combine_to_host",
     "accumulate_stats", "dispatch_sf_col_major", "new_sf_col_major", "sf_col_major_ld",
     "dispatch_permute", "combine_unpermute", "get_error", "kernel_launches", "strerror",
-    "library_path", "load_library", "dispatch", "ERROR_NAMES",
+    "library_path", "load_library", "dispatch", "ERROR_NAMES", "HostPipeline",
 )
 
 __all__ = list(_BINDING_NAMES) + ["workloads"]

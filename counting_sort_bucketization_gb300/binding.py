@@ -434,6 +434,91 @@ class Layout:
         return get_error(self.workspace, stream)
 
 
+class HostPipeline:
+    """Batches from host memory through dispatch, an expert step and combine
+    back to host memory, with ``lanes`` batches in flight.
+
+    Each lane owns a layout (with its workspace), device buffers and a pair
+    of streams.  Batch i runs on lane i % lanes: ``dispatch_from_host``, then
+    ``expert(layout, recv_x, recv_sf)`` (called on the lane's stream; it
+    returns the bf16 expert outputs in receive-row order), then
+    ``combine_to_host``; with ``expert=None`` the batch is a dispatch only and
+    its receive rows come back to ``out_host`` instead (same shape and dtype
+    as the lane's receive buffer).  Batches on different lanes are independent, so one
+    batch's copy back to the host overlaps the next batch's copy in: the host
+    link carries both directions at once.  ``submit`` returns an event that
+    completes when the batch's result is in ``out_host``; until then the
+    batch's host buffers must stay untouched.  A lane is reused only after
+    its previous batch, by stream order.
+    """
+
+    def __init__(self, desc, capacity_rows: int, hidden: int, x_dtype=torch.bfloat16, sf_cols: int = 0,
+                 lanes: int = 2, chunk_tokens: int = 0, device="cuda"):
+        if lanes < 1:
+            raise ValueError("lanes must be >= 1")
+        N, K = int(desc.num_tokens), int(desc.topk)
+        self.desc, self.chunk_tokens, self.device = desc, int(chunk_tokens), torch.device(device)
+        self._lanes = []
+        for _ in range(lanes):
+            lane = {
+                "layout": Layout(desc, capacity_rows, device=device),
+                "topk_idx": torch.empty((N, K), dtype=torch.int64, device=device),
+                "x": torch.empty((N, hidden), dtype=x_dtype, device=device),
+                "recv": torch.empty((int(capacity_rows), hidden), dtype=x_dtype, device=device),
+                "weights": torch.empty((N, K), dtype=torch.float32, device=device),
+                "sf": torch.empty((N, sf_cols), dtype=torch.float32, device=device) if sf_cols else None,
+                "recv_sf": torch.empty((int(capacity_rows), sf_cols), dtype=torch.float32, device=device)
+                if sf_cols else None,
+                "out": None,
+                "stream": torch.cuda.Stream(device),
+                "copy": torch.cuda.Stream(device),
+            }
+            self._lanes.append(lane)
+        self._next = 0
+
+    @property
+    def lanes(self) -> int:
+        return len(self._lanes)
+
+    def lane(self, i: int) -> dict:
+        return self._lanes[i]
+
+    def submit(self, topk_idx_host, x_host, weights_host, out_host, expert, sf_host=None) -> torch.cuda.Event:
+        lane = self._lanes[self._next]
+        self._next = (self._next + 1) % len(self._lanes)
+        s, cs, lay = lane["stream"], lane["copy"], lane["layout"]
+        # The lane's stream starts after whatever the caller enqueued so far.
+        s.wait_stream(torch.cuda.current_stream(self.device))
+        dispatch_from_host(lay, topk_idx_host, x_host, lane["topk_idx"], lane["x"], lane["recv"],
+                           weights_host=weights_host, weights=lane["weights"], sf_host=sf_host, sf=lane["sf"],
+                           recv_sf=lane["recv_sf"], chunk_tokens=self.chunk_tokens, stream=s, copy_stream=cs)
+        if expert is None:
+            cs.wait_stream(s)
+            with torch.cuda.stream(cs):
+                out_host.copy_(lane["recv"], non_blocking=True)
+            s.wait_stream(cs)
+        else:
+            with torch.cuda.stream(s):
+                eo = expert(lay, lane["recv"], lane["recv_sf"])
+                if lane["out"] is None or lane["out"].shape != out_host.shape:
+                    lane["out"] = torch.empty(out_host.shape, dtype=torch.bfloat16, device=self.device)
+            combine_to_host(lay, eo, lane["weights"], lane["out"], out_host, chunk_tokens=self.chunk_tokens,
+                            stream=s, copy_stream=cs)
+        done = torch.cuda.Event()
+        done.record(s)
+        return done
+
+    def join(self, stream=None) -> None:
+        """Make ``stream`` (default: the current one) wait for every submitted batch."""
+        st = stream if stream is not None else torch.cuda.current_stream(self.device)
+        for lane in self._lanes:
+            st.wait_stream(lane["stream"])
+
+    def errors(self) -> list[int]:
+        """Each lane's sticky device error (synchronises the lanes)."""
+        return [lane["layout"].error(lane["stream"]) for lane in self._lanes]
+
+
 def dispatch(topk_idx, x, num_experts, num_ranks, alignment, sf=None, capacity_rows=None, stream=None):
     """Count, scan and permute in one call; returns ``(layout, recv_x, recv_sf)``.
 

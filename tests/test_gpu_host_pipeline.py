@@ -80,3 +80,44 @@ def test_fp8_rows_with_scale_factors():
 
 def test_masked_and_ragged():
     pipeline_case(wl.Workload("edge", 777, 4, 24, 6, 8, 64, mask_prob=0.3), 7, 100)
+
+
+def stand_in_expert(scale_d):
+    """Rows of expert e's segment scaled by scale[e] (fp32 product, one bf16 rounding); gap rows stay 0."""
+    def expert(lay, recv, recv_sf):
+        rows = recv.shape[0]
+        off = lay.expert_offset.to(torch.int64)
+        row_e = torch.searchsorted(off[1:], torch.arange(rows, device=recv.device), right=True)
+        row_e = row_e.clamp(max=scale_d.shape[0] - 1)
+        return (recv.float() * scale_d[row_e][:, None]).to(torch.bfloat16)
+    return expert
+
+
+def oracle_batch(inp, w):
+    ref = oracle.layout(inp["topk_idx"].numpy(), w.num_experts, w.num_ranks, w.alignment)
+    rows = ref["total_rows"]
+    _, recv, _ = oracle.permute(u8(inp["x"]), ref["dst_slot"], ref["expert_offset"], ref["expert_count"], rows)
+    eo = oracle.expert_scale(recv.view(np.uint16).reshape(rows, w.hidden), ref["expert_offset"],
+                             inp["expert_scale"].numpy())
+    return oracle.combine(eo, ref["dst_slot"], inp["weights"].numpy())
+
+
+@pytest.mark.parametrize("lanes", [1, 2, 3])
+@pytest.mark.parametrize("name,chunk", [("tiny", 100), ("decode", 1024)])
+def test_pipelined_batches(name, chunk, lanes):
+    # five different batches, several in flight at once; each result equals the oracle's
+    w = wl.WORKLOADS[name]
+    if name == "decode":
+        w = w.replace(num_tokens=1536)
+    cap = wl.worst_case_rows(w)
+    pipe = binding.HostPipeline(w, cap, w.hidden, lanes=lanes, chunk_tokens=chunk, device=DEV)
+    expert = stand_in_expert(wl.expert_scale(w).to(DEV))
+    batches = [wl.make(w, 20 + b) for b in range(5)]
+    host = [(b["topk_idx"].pin_memory(), b["x"].pin_memory(), b["weights"].pin_memory()) for b in batches]
+    outs = [torch.full((w.num_tokens, w.hidden), 5.0, dtype=torch.bfloat16).pin_memory() for _ in batches]
+    done = [pipe.submit(i, x, wt, o, expert) for (i, x, wt), o in zip(host, outs)]
+    for ev in done:
+        ev.synchronize()
+    assert pipe.errors() == [0] * lanes
+    for b, o in zip(batches, outs):
+        np.testing.assert_array_equal(o.view(torch.int16).numpy().view(np.uint16), oracle_batch(b, w))
