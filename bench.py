@@ -41,8 +41,8 @@ L2_FLUSH_BYTES = 256 << 20          # > 2x the 129 MB L2
 # DRAM traffic of the permute kernel from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), per launch, scaled to the decode workload, tied to
 # the kernel sources it was measured on.  bench reports null if they changed.
-PERMUTE_TRAFFIC = {"sha256": "78e49d470fbe4630e851b31cfd7452435e1b5bec1d43ac7675a112b40573dd5a",
-                   "workload": "decode", "bytes_per_launch": 58_954_240 + 646_191_872}
+PERMUTE_TRAFFIC = {"sha256": "317cdf765d3bea4a449fce5a32370637b99eb2f51dd0b94fb791d6ddb0a419fb",
+                   "workload": "decode", "bytes_per_launch": 58_919_424 + 648_130_304}
 PERMUTE_SOURCES = ["counting_sort_bucketization_gb300/csrc/permute_kernel.cu",
                    "counting_sort_bucketization_gb300/csrc/ptx.cuh",
                    "counting_sort_bucketization_gb300/csrc/common.cuh"]

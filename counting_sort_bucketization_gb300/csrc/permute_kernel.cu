@@ -54,6 +54,20 @@ constexpr int kStageBudgetBytes = MOE_PERMUTE_STAGE_BUDGET;  // shared-memory ri
 constexpr int kCtasPerSm = MOE_PERMUTE_CTAS_PER_SM;           // static kernel's grid target
 constexpr int kMaxTokensPerCta = 512;
 constexpr int kSfRegWords = 4;  // scale-factor words a lane keeps in registers
+#ifndef MOE_PERMUTE_MIN_UNIT_BYTES
+#define MOE_PERMUTE_MIN_UNIT_BYTES 3584
+#endif
+#ifndef MOE_PERMUTE_UNITS_PER_CTA
+#define MOE_PERMUTE_UNITS_PER_CTA 48
+#endif
+// The dynamic kernel cuts rows into the fewest pieces that give each CTA at
+// least kUnitsPerCta units, but no piece below kMinUnitBytes: a sweep of
+// fixed piece sizes on GB300 put decode-sized batches (6-7 rows per CTA) at
+// 0.88 of the copy peak with whole rows and 0.94 with 3.5 KB pieces, while
+// pieces of 2 KB lost up to 12 % on the large batches.
+constexpr int kMinUnitBytes = MOE_PERMUTE_MIN_UNIT_BYTES;
+constexpr int kUnitsPerCta = MOE_PERMUTE_UNITS_PER_CTA;
+static_assert(kMinUnitBytes >= 16 && kMinUnitBytes % 16 == 0, "piece size");
 
 __device__ __forceinline__ int warp_inclusive_scan(int v, int lane) {
 #pragma unroll
@@ -334,11 +348,18 @@ PermutePlan make_permute_plan(const PermuteArgs& a, int sms) {
 }
 
 // ------------------------------------------------------ dynamic (default)
+// The unit of work is a piece of one token row (a "unit": the row cut into
+// `pieces` of at most unit_bytes): a CTA holds several units in its ring
+// for the bandwidth, and small units keep most of them in the shared
+// counter, where whichever CTA is free first takes them.  With whole rows
+// as units the first claims alone handed out ~3/4 of a 4096-token batch.
 struct DynPlan {
   int row_bytes;     // <= kMaxChunkBytes, multiple of 16
+  int unit_bytes;    // row bytes a unit moves (multiple of 16); the last piece of a row may be shorter
+  int pieces;        // units per row
   int slot_win;      // bytes reserved per stage for the token's 16-byte-aligned slot window
-  int sf_bytes;      // scale-factor row bytes (multiple of 16) or 0
-  int stage_bytes;   // row + slot window + scale row, rounded to 128
+  int sf_bytes;      // scale-factor row bytes (multiple of 16) or 0; moved with piece 0
+  int stage_bytes;   // unit + slot window + scale row, rounded to 128
   int stages;
   int64_t grid;
   size_t off_padpre, smem;
@@ -366,6 +387,7 @@ __global__ void __launch_bounds__(kPermuteThreads)
 
   // ---- the CTA's TMA thread ---------------------------------------------
   const int64_t N = a.num_tokens;
+  const int64_t U = N * p.pieces;   // units: piece c of token t is unit t * pieces + c
   const int64_t rb = a.row_bytes, srb = a.sf_row_bytes;
   const int S = p.stages;
   const int64_t G = gridDim.x;
@@ -384,20 +406,33 @@ __global__ void __launch_bounds__(kPermuteThreads)
   for (int s = 0; s < S; ++s) ptx::mbar_init(&full_bar[s], 1);
   ptx::fence_mbar_init();
 
-  // The first S tokens of every CTA are fixed (blockIdx.x + i*G): their rows
+  // Unit u: token u / pieces, bytes [off, off + len) of its row; piece 0
+  // also carries the token's scale row.
+  auto piece_of = [&](int64_t u, int64_t& t, int64_t& off, uint32_t& len, bool& with_sf) {
+    t = u / p.pieces;
+    const int c = static_cast<int>(u - t * p.pieces);
+    off = static_cast<int64_t>(c) * p.unit_bytes;
+    len = static_cast<uint32_t>(min64(p.unit_bytes, rb - off));
+    with_sf = p.sf_bytes != 0 && c == 0;
+  };
+  // The first S units of every CTA are fixed (blockIdx.x + i*G): their rows
   // and scale rows do not depend on the layout, so they are requested before
   // waiting for the previous kernel.  Each stage's phase completes only after
   // the post-wait arrival, which also brings the slot window.
   int npre = 0;
   for (; npre < S; ++npre) {
-    const int64_t t = blockIdx.x + npre * G;
-    if (t >= N) break;
+    const int64_t u = blockIdx.x + npre * G;
+    if (u >= U) break;
+    int64_t t, off;
+    uint32_t len;
+    bool with_sf;
+    piece_of(u, t, off, len, with_sf);
     uint8_t* st = smem + static_cast<size_t>(npre) * p.stage_bytes;
-    stage_tok[npre] = t;
-    ptx::mbar_expect_tx(&full_bar[npre], static_cast<uint32_t>(rb + p.sf_bytes));
-    ptx::bulk_g2s(st, a.x + t * rb, static_cast<uint32_t>(rb), &full_bar[npre]);
-    if (p.sf_bytes)
-      ptx::bulk_g2s(st + p.row_bytes + p.slot_win, a.sf + t * srb, static_cast<uint32_t>(p.sf_bytes),
+    stage_tok[npre] = u;
+    ptx::mbar_expect_tx(&full_bar[npre], len + (with_sf ? static_cast<uint32_t>(p.sf_bytes) : 0u));
+    ptx::bulk_g2s(st, a.x + t * rb + off, len, &full_bar[npre]);
+    if (with_sf)
+      ptx::bulk_g2s(st + p.unit_bytes + p.slot_win, a.sf + t * srb, static_cast<uint32_t>(p.sf_bytes),
                     &full_bar[npre]);
   }
   ptx::grid_dependency_wait();
@@ -411,43 +446,47 @@ __global__ void __launch_bounds__(kPermuteThreads)
   }
   for (int i = 0; i < npre; ++i) {
     uintptr_t w0, w1, first;
-    if (window_of(stage_tok[i], w0, w1, first)) {
+    if (window_of(stage_tok[i] / p.pieces, w0, w1, first)) {
       ptx::mbar_arrive_expect_tx(&full_bar[i], static_cast<uint32_t>(w1 - w0));
-      ptx::bulk_g2s(smem + static_cast<size_t>(i) * p.stage_bytes + p.row_bytes, reinterpret_cast<const void*>(w0),
+      ptx::bulk_g2s(smem + static_cast<size_t>(i) * p.stage_bytes + p.unit_bytes, reinterpret_cast<const void*>(w0),
                     static_cast<uint32_t>(w1 - w0), &full_bar[i]);
     } else {
       ptx::mbar_arrive(&full_bar[i]);
     }
   }
 
-  // Later tokens are claimed from the counter (claim c is token G*S + c),
+  // Later units are claimed from the counter (claim c is unit G*S + c),
   // two claims ahead of use so the atomic's latency is hidden.
   const int64_t claimed_base = G * S;
   int64_t claim0 = claimed_base + atomicAdd(next_tok, 1u), claim1 = claimed_base + atomicAdd(next_tok, 1u);
   bool exhausted = npre < S;
   int64_t issued = npre;
   auto issue = [&]() {
-    const int64_t t = claim0;
+    const int64_t u = claim0;
     claim0 = claim1;
-    if (t >= N) {
+    if (u >= U) {
       exhausted = true;
       return;
     }
     claim1 = claimed_base + atomicAdd(next_tok, 1u);
+    int64_t t, off;
+    uint32_t len;
+    bool with_sf;
+    piece_of(u, t, off, len, with_sf);
     const int s = static_cast<int>(issued % S);
     uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
-    stage_tok[s] = t;
+    stage_tok[s] = u;
     uintptr_t w0, w1, first;
     const bool window = window_of(t, w0, w1, first);
-    const uint32_t tx = static_cast<uint32_t>(rb) + (window ? static_cast<uint32_t>(w1 - w0) : 0u) +
-                        static_cast<uint32_t>(p.sf_bytes);
+    const uint32_t tx = len + (window ? static_cast<uint32_t>(w1 - w0) : 0u) +
+                        (with_sf ? static_cast<uint32_t>(p.sf_bytes) : 0u);
     ptx::mbar_arrive_expect_tx(&full_bar[s], tx);
-    ptx::bulk_g2s(st, a.x + t * rb, static_cast<uint32_t>(rb), &full_bar[s]);
+    ptx::bulk_g2s(st, a.x + t * rb + off, len, &full_bar[s]);
     if (window)
-      ptx::bulk_g2s(st + p.row_bytes, reinterpret_cast<const void*>(w0), static_cast<uint32_t>(w1 - w0),
+      ptx::bulk_g2s(st + p.unit_bytes, reinterpret_cast<const void*>(w0), static_cast<uint32_t>(w1 - w0),
                     &full_bar[s]);
-    if (p.sf_bytes)
-      ptx::bulk_g2s(st + p.row_bytes + p.slot_win, a.sf + t * srb, static_cast<uint32_t>(p.sf_bytes), &full_bar[s]);
+    if (with_sf)
+      ptx::bulk_g2s(st + p.unit_bytes + p.slot_win, a.sf + t * srb, static_cast<uint32_t>(p.sf_bytes), &full_bar[s]);
     ++issued;
   };
   int64_t j = 0;
@@ -458,21 +497,24 @@ __global__ void __launch_bounds__(kPermuteThreads)
       ok = false;
       break;
     }
-    const int64_t t = stage_tok[s];
+    int64_t t, off;
+    uint32_t len;
+    bool with_sf;
+    piece_of(stage_tok[s], t, off, len, with_sf);
     const uint8_t* st = smem + static_cast<size_t>(s) * p.stage_bytes;
     uintptr_t w0, w1, first;
     const bool window = window_of(t, w0, w1, first);
-    const int32_t* sl = window ? reinterpret_cast<const int32_t*>(st + p.row_bytes + (first - w0)) : nullptr;
+    const int32_t* sl = window ? reinterpret_cast<const int32_t*>(st + p.unit_bytes + (first - w0)) : nullptr;
     for (int k = 0; k < K; ++k) {
       const int32_t slot = window ? sl[k] : __ldg(a.dst_slot + t * K + k);
       if (slot < 0) continue;
       if (slot >= a.capacity) {
-        set_error(a.err, MOE_ERR_CAPACITY);
+        if (off == 0) set_error(a.err, MOE_ERR_CAPACITY);
         continue;
       }
-      ptx::bulk_s2g(a.recv_x + slot * rb, st, static_cast<uint32_t>(rb));
-      if (p.sf_bytes)
-        ptx::bulk_s2g(a.recv_sf + slot * srb, st + p.row_bytes + p.slot_win, static_cast<uint32_t>(srb));
+      ptx::bulk_s2g(a.recv_x + slot * rb + off, st, len);
+      if (with_sf)
+        ptx::bulk_s2g(a.recv_sf + slot * srb, st + p.unit_bytes + p.slot_win, static_cast<uint32_t>(srb));
     }
     ptx::bulk_commit();
     if (!exhausted) {
@@ -495,8 +537,12 @@ __global__ void __launch_bounds__(kPermuteThreads)
   }
 }
 
+int max_pieces(const PermuteArgs& a) { return static_cast<int>(max64(1, ceil_div64(a.row_bytes, kMinUnitBytes))); }
+
 bool dyn_applicable(const PermuteArgs& a) {
   if (a.row_bytes > kMaxChunkBytes || a.work == nullptr) return false;
+  // Unit indices (and the claims past them) must fit the 32-bit counter.
+  if (a.num_tokens * max_pieces(a) >= (int64_t{1} << 31)) return false;
   if (a.sf != nullptr) {
     if (a.sf_row_bytes % 16 != 0 || a.sf_row_bytes > 4096) return false;
     if (reinterpret_cast<uintptr_t>(a.sf) % 16 != 0 || reinterpret_cast<uintptr_t>(a.recv_sf) % 16 != 0) return false;
@@ -504,12 +550,17 @@ bool dyn_applicable(const PermuteArgs& a) {
   return true;
 }
 
-DynPlan make_dyn_plan(const PermuteArgs& a) {
+// Plan for rows cut into (about) `pieces` equal 16-byte-multiple pieces; the
+// piece count is recomputed from the rounded size, so the last piece is
+// never empty.
+DynPlan make_dyn_plan(const PermuteArgs& a, int pieces) {
   DynPlan p{};
   p.row_bytes = static_cast<int>(a.row_bytes);
+  p.unit_bytes = static_cast<int>(ceil_div64(ceil_div64(a.row_bytes, max64(1, pieces)), 16) * 16);
+  p.pieces = static_cast<int>(ceil_div64(a.row_bytes, p.unit_bytes));
   p.slot_win = static_cast<int>((4 * a.topk + 32 + 15) / 16 * 16);
   p.sf_bytes = a.sf != nullptr ? static_cast<int>(a.sf_row_bytes) : 0;
-  p.stage_bytes = (p.row_bytes + p.slot_win + p.sf_bytes + 127) / 128 * 128;
+  p.stage_bytes = (p.unit_bytes + p.slot_win + p.sf_bytes + 127) / 128 * 128;
   p.stages = std::max(2, std::min(kMaxStages, kStageBudgetBytes / p.stage_bytes));
   size_t off = static_cast<size_t>(p.stages) * p.stage_bytes;
   p.off_padpre = off;
@@ -521,19 +572,23 @@ DynPlan make_dyn_plan(const PermuteArgs& a) {
 // CTAs of the dynamic kernel resident per SM at this shared-memory size (cached).
 int dyn_ctas_per_sm(size_t smem) {
   static std::mutex mu;
-  static size_t cached_smem[8] = {};
-  static int cached_occ[8] = {};
-  static int cached_dev[8] = {};
+  constexpr int kSlots = 32;
+  static size_t cached_smem[kSlots] = {};
+  static int cached_occ[kSlots] = {};
+  static int cached_dev[kSlots] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;
   std::lock_guard<std::mutex> lock(mu);
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < kSlots; ++i)
     if (cached_occ[i] > 0 && cached_smem[i] == smem && cached_dev[i] == dev) return cached_occ[i];
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, permute_dyn_kernel, kPermuteThreads, smem) != cudaSuccess ||
+  // The occupancy of a size above 48 KB counts only once the kernel may use it.
+  if (cudaFuncSetAttribute(permute_dyn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, permute_dyn_kernel, kPermuteThreads, smem) != cudaSuccess ||
       occ < 1)
     occ = 1;
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < kSlots; ++i)
     if (cached_occ[i] == 0) {
       cached_smem[i] = smem;
       cached_occ[i] = occ;
@@ -547,12 +602,18 @@ int dyn_ctas_per_sm(size_t smem) {
 
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t stream) {
   if (dyn_applicable(a)) {
-    DynPlan p = make_dyn_plan(a);
+    DynPlan p = make_dyn_plan(a, 1);
+    int64_t resident = static_cast<int64_t>(dyn_ctas_per_sm(p.smem)) * device_sm_count();
+    const int64_t want = ceil_div64(kUnitsPerCta * resident, max64(1, a.num_tokens));
+    const int pieces = static_cast<int>(min64(want, max_pieces(a)));
+    if (pieces > 1) {
+      p = make_dyn_plan(a, pieces);
+      resident = static_cast<int64_t>(dyn_ctas_per_sm(p.smem)) * device_sm_count();
+    }
     cudaError_t st = cudaFuncSetAttribute(permute_dyn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           static_cast<int>(p.smem));
     if (st != cudaSuccess) return st;
-    const int64_t resident = static_cast<int64_t>(dyn_ctas_per_sm(p.smem)) * device_sm_count();
-    p.grid = max64(1, min64(resident, a.num_tokens));
+    p.grid = max64(1, min64(resident, a.num_tokens * p.pieces));
     st = launch_pdl(permute_dyn_kernel, dim3(static_cast<unsigned>(p.grid)), dim3(kPermuteThreads), p.smem, stream,
                     a, p);
     if (st != cudaSuccess) return st;
