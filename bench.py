@@ -41,7 +41,7 @@ L2_FLUSH_BYTES = 256 << 20          # > 2x the 129 MB L2
 # DRAM traffic of the permute kernel from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), per launch, scaled to the decode workload, tied to
 # the kernel sources it was measured on.  bench reports null if they changed.
-PERMUTE_TRAFFIC = {"sha256": "317cdf765d3bea4a449fce5a32370637b99eb2f51dd0b94fb791d6ddb0a419fb",
+PERMUTE_TRAFFIC = {"sha256": "745fb26f1f2550464134191aa72b5d0a37bf141660ffbd823598ebf87022be0c",
                    "workload": "decode", "bytes_per_launch": 58_919_424 + 648_130_304}
 PERMUTE_SOURCES = ["counting_sort_bucketization_gb300/csrc/permute_kernel.cu",
                    "counting_sort_bucketization_gb300/csrc/ptx.cuh",
@@ -315,20 +315,22 @@ def run_native(args, rank, world, local):
         flush_w.zero_()
         flush_r.max()
 
+    # The step's kernels in order, one event after each (and one before the
+    # first): every timed interval holds exactly one step of the path.
+    stages = [("layout", lambda: lay.build(idx_d)),
+              ("permute", lambda: lay.permute(x_d, recv, perm_sf, perm_recv_sf))]
+    if sf_cm:
+        stages.append(("sf_col_major", lambda: lay.permute_sf_col_major(sf_d, recv_sf_cm)))
+    if do_combine:
+        stages.append(("combine", lambda: lay.combine(eo, wt_d, out)))
+
     def step(ev):
         ev[0].record(stream)
-        lay.build(idx_d)
-        ev[1].record(stream)
-        lay.permute(x_d, recv, perm_sf, perm_recv_sf)
-        ev[2].record(stream)
-        if sf_cm:
-            lay.permute_sf_col_major(sf_d, recv_sf_cm)
-        ev[3].record(stream)
-        if do_combine:
-            lay.combine(eo, wt_d, out)
-        ev[4].record(stream)
+        for i, (_, run) in enumerate(stages):
+            run()
+            ev[i + 1].record(stream)
 
-    new_events = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    new_events = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
     for _ in range(args.warmup):
         flush_l2()
         step(new_events())
@@ -355,13 +357,13 @@ def run_native(args, rank, world, local):
     err = lay.error()
     assert err == 0, f"device error {err} in the timed region"
 
-    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(4)] for e in evs])   # ms
+    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(len(stages))] for e in evs])   # ms
     step_ms = per.sum(axis=1)
     ms_per_step = reduce_max(float(step_ms.mean()), world, dev)
-    kern_ms = per.mean(axis=0)     # layout (count + scan + rank), permute, column-major scales, combine
+    kern_ms = dict(zip([name for name, _ in stages], per.mean(axis=0).tolist()))
     ab = algorithmic_bytes(w, lay, sf_cm)
     value = world * N / (ms_per_step / 1e3)
-    dispatch_ms = float(kern_ms[:3].sum())
+    dispatch_ms = kern_ms["layout"] + kern_ms["permute"] + kern_ms.get("sf_col_major", 0.0)
 
     # End to end through the public API with host buffers: pinned ids, rows
     # and weights in, the combined tokens back (dispatch-only workloads: the
@@ -407,7 +409,7 @@ def run_native(args, rank, world, local):
     if rank != 0:
         return
     peaks = measured_peaks()
-    permute_s = kern_ms[1] / 1e3
+    permute_s = kern_ms["permute"] / 1e3
     achieved = ab["permute"] / permute_s / 1e9
     traffic = None
     if PERMUTE_TRAFFIC and PERMUTE_TRAFFIC.get("sha256") == sources_sha256(PERMUTE_SOURCES) \
@@ -420,12 +422,11 @@ def run_native(args, rank, world, local):
         "roofline": {"kernel": "permute_dyn_kernel", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "peak_source": peaks["source"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "traffic": traffic, "algorithmic_bytes_per_launch": ab["permute"]},
-        "kernels_ms": {"layout": kern_ms[0], "permute": kern_ms[1],
-                       "sf_col_major": kern_ms[2] if sf_cm else None,
-                       "combine": kern_ms[3] if do_combine else None},
+        "kernels_ms": {"layout": kern_ms["layout"], "permute": kern_ms["permute"],
+                       "sf_col_major": kern_ms.get("sf_col_major"), "combine": kern_ms.get("combine")},
         "kernels_gbs": {"permute": ab["permute"] / permute_s / 1e9,
-                        "sf_col_major": (ab["sf_col_major"] / (kern_ms[2] / 1e3) / 1e9) if sf_cm else None,
-                        "combine": (ab["combine"] / (kern_ms[3] / 1e3) / 1e9) if do_combine else None},
+                        "sf_col_major": (ab["sf_col_major"] / (kern_ms["sf_col_major"] / 1e3) / 1e9) if sf_cm else None,
+                        "combine": (ab["combine"] / (kern_ms["combine"] / 1e3) / 1e9) if do_combine else None},
         "dispatch_tokens_per_s": world * N / (dispatch_ms / 1e3),
         "layout": {"valid_pairs": ab["P"], "rows": ab["rows"], "tokens_routed": ab["tokens_routed"]},
         "e2e": {"value": world * N / (e2e_step_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,

@@ -376,28 +376,25 @@ __global__ void __launch_bounds__(kLayoutThreads)
   rank_phase(plan, a, blockIdx.x, tc, ids_s, off_s, cnt_s, lr_s, warp_tot_s);
 }
 
-// Grid-wide barrier for a cooperative launch: arrive on a counter; the last
-// CTA resets it and bumps the generation the others wait on.  The wait is
-// bounded; on timeout the error word gets MOE_ERR_TIMEOUT and the CTA stops.
-__device__ bool grid_barrier(unsigned* arrive, unsigned* gen, unsigned nctas, int* err, int* flag_s) {
+// Grid-wide barrier for a cooperative launch on a counter that only grows
+// within the launch: barrier b (1, 2, ...) is passed once the counter holds
+// b * gridDim.x arrivals, so a barrier costs one atomic and the polls.  Each
+// CTA arrives once more when it leaves (grid_exit); the last of those
+// arrivals resets the counter for the next launch on the workspace.  The
+// wait is bounded; on timeout the error word gets MOE_ERR_TIMEOUT and the CTA
+// stops (the counter then stays set: the workspace must be zeroed again).
+__device__ bool grid_barrier(unsigned* count, unsigned target, int* err, int* flag_s) {
   __syncthreads();
   if (threadIdx.x == 0) {
     bool ok = true;
-    const unsigned g0 = ptx::ld_acquire_gpu(gen);
-    __threadfence();
-    if (atomicAdd(arrive, 1u) == nctas - 1) {
-      atomicExch(arrive, 0u);
-      __threadfence();
-      atomicAdd(gen, 1u);
-    } else {
-      const uint64_t t0 = ptx::globaltimer_ns();
-      while (ptx::ld_acquire_gpu(gen) == g0) {
-        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
-          set_error(err, MOE_ERR_TIMEOUT);
-          ok = false;
-          break;
-        }
-        __nanosleep(64);
+    __threadfence();   // the CTA's writes before the barrier, then the arrival
+    atomicAdd(count, 1u);
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (ptx::ld_acquire_gpu(count) < target) {
+      if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+        set_error(err, MOE_ERR_TIMEOUT);
+        ok = false;
+        break;
       }
     }
     __threadfence();
@@ -405,6 +402,11 @@ __device__ bool grid_barrier(unsigned* arrive, unsigned* gen, unsigned nctas, in
   }
   __syncthreads();
   return *flag_s != 0;
+}
+
+// Last arrival: every CTA has passed all `barriers` barriers; reset the counter.
+__device__ void grid_exit(unsigned* count, unsigned barriers) {
+  if (threadIdx.x == 0 && atomicAdd(count, 1u) == (barriers + 1) * gridDim.x - 1) atomicExch(count, 0u);
 }
 
 template <typename IdT>
@@ -439,9 +441,10 @@ __global__ void __launch_bounds__(kLayoutThreads)
     hist[static_cast<int64_t>(e) * T + tile] = c;
   }
   for (int r = threadIdx.x; r < R; r += blockDim.x) rhist[static_cast<int64_t>(r) * T + tile] = rhist_s[r];
-  if (!grid_barrier(bar, bar + 1, gridDim.x, a.err, &flag_s)) return;
+  if (!grid_barrier(bar, gridDim.x, a.err, &flag_s)) return;
   scan_phase(hist, rhist, plan.tiles, E, R, expert_count, rank_count);
-  if (!grid_barrier(bar, bar + 1, gridDim.x, a.err, &flag_s)) return;
+  if (!grid_barrier(bar, 2 * gridDim.x, a.err, &flag_s)) return;
+  grid_exit(bar, 2);
   rank_finish(plan, a, tile, tc, ids_s, off_s, cnt_s, lr_s, warp_tot_s);
 }
 
@@ -688,12 +691,21 @@ cudaError_t launch_rank_rows_t(const moe_layout_desc& d, const TilePlan& p, cons
   return cudaSuccess;
 }
 
+bool& fused_pdl_refused() {
+  static bool refused = false;
+  return refused;
+}
+
 template <typename IdT>
 cudaError_t launch_build_t(const moe_layout_desc& d, const TilePlan& p, const IdT* topk_idx, int32_t* expert_count,
                            int32_t* rank_count, int32_t* hist, int32_t* rhist, unsigned* barrier_words,
                            const RankArgs& a, cudaStream_t stream) {
   const size_t smem = fused_smem_bytes(d, p);
-  if (!fused_fits<IdT>(p, smem)) {
+  // With one chunk per warp (up to ~64k pairs) the three PDL-chained kernels
+  // measured faster on GB300 than the cooperative kernel's two grid barriers
+  // (decode: 13.7 vs 14.5 us); from two chunks per warp on, the fused kernel
+  // wins (32768 x 8 ids: 19.6 vs 21.3 us; 131072 x 8: 37.1 vs 50.4 us).
+  if (p.cpw < 2 || !fused_fits<IdT>(p, smem)) {
     cudaError_t st = launch_count_t(d, p, topk_idx, expert_count, rank_count, a.err, hist, rhist, stream);
     if (st != cudaSuccess) return st;
     return launch_rank_t(d, p, topk_idx, a, stream);
@@ -703,13 +715,25 @@ cudaError_t launch_build_t(const moe_layout_desc& d, const TilePlan& p, const Id
   cfg.blockDim = dim3(kLayoutThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  // Cooperative, and allowed to start during the previous kernel's tail (it
+  // waits with griddepcontrol.wait before reading anything).  A driver that
+  // refuses the pair gets the plain cooperative launch.
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t st = cudaLaunchKernelEx(&cfg, layout_fused_kernel<IdT>, topk_idx, p, a, hist, rhist,
-                                            expert_count, rank_count, barrier_words);
+  cfg.numAttrs = fused_pdl_refused() ? 1 : 2;
+  cudaError_t st = cudaLaunchKernelEx(&cfg, layout_fused_kernel<IdT>, topk_idx, p, a, hist, rhist, expert_count,
+                                      rank_count, barrier_words);
+  if (st != cudaSuccess && cfg.numAttrs == 2) {
+    (void)cudaGetLastError();
+    fused_pdl_refused() = true;
+    cfg.numAttrs = 1;
+    st = cudaLaunchKernelEx(&cfg, layout_fused_kernel<IdT>, topk_idx, p, a, hist, rhist, expert_count, rank_count,
+                            barrier_words);
+  }
   if (st != cudaSuccess) return st;
   count_launch();
   return cudaSuccess;

@@ -189,6 +189,8 @@ EDGE = [
     _w(5000, 8, 256, 8, 128, routing="zipf", zipf_s=2.5, mask_prob=0.1, H=32),  # extreme skew
     _w(40, 2, 8, 2, 4, H=8192 * 2),              # rows wider than one 16 KiB bulk slice
     _w(129, 8, 16, 4, 4, H=384, row_dtype="fp8"),  # fp8 rows, 12-byte scale-factor rows
+    _w(40007, 3, 40, 5, 16, H=16),               # one-call layout in the cooperative kernel, ragged last tile
+    _w(70001, 1, 64, 8, 4, H=16),                # the same with K = 1
 ]
 
 
@@ -321,8 +323,13 @@ def test_kernel_launch_counter_moves():
     before = binding.kernel_launches()
     full_case(wl.WORKLOADS["tiny"], 0, fused=False)
     assert binding.kernel_launches() - before == 5     # count, column scan, rank, permute, combine
+    # One-call build: the same three chained kernels while a tile holds one chunk per warp ...
     before = binding.kernel_launches()
     full_case(wl.WORKLOADS["tiny"], 0, fused=True)
+    assert binding.kernel_launches() - before == 5
+    # ... and the cooperative kernel from two chunks per warp on
+    before = binding.kernel_launches()
+    full_case(_w(40007, 3, 40, 5, 16, H=16), 1, fused=True)
     assert binding.kernel_launches() - before == 3     # fused layout, permute, combine
 
 
