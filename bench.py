@@ -498,7 +498,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=list(wl.WORKLOADS), default="decode")
     ap.add_argument("--e2e-steps", type=int, default=50)
-    ap.add_argument("--e2e-chunks", type=int, default=4, help="token chunks the host copies are split into")
+    ap.add_argument("--e2e-chunks", type=int, default=2, help="token chunks the host copies are split into")
     ap.add_argument("--e2e-lanes", type=int, default=3, help="batches in flight in the end-to-end leg")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-max-passes", type=int, default=20)
