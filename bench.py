@@ -41,8 +41,8 @@ L2_FLUSH_BYTES = 256 << 20          # > 2x the 129 MB L2
 # DRAM traffic of the permute kernel from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), per launch, scaled to the decode workload, tied to
 # the kernel sources it was measured on.  bench reports null if they changed.
-PERMUTE_TRAFFIC = {"sha256": "745fb26f1f2550464134191aa72b5d0a37bf141660ffbd823598ebf87022be0c",
-                   "workload": "decode", "bytes_per_launch": 58_919_424 + 648_130_304}
+PERMUTE_TRAFFIC = {"sha256": "0efef350c87eaeede7a793591d2220baf5a66b545748de0f9b43e958cea03f58",
+                   "workload": "decode", "bytes_per_launch": 58_910_208 + 647_979_776}
 PERMUTE_SOURCES = ["counting_sort_bucketization_gb300/csrc/permute_kernel.cu",
                    "counting_sort_bucketization_gb300/csrc/ptx.cuh",
                    "counting_sort_bucketization_gb300/csrc/common.cuh"]

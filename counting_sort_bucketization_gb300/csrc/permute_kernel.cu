@@ -65,9 +65,35 @@ constexpr int kSfRegWords = 4;  // scale-factor words a lane keeps in registers
 // fixed piece sizes on GB300 put decode-sized batches (6-7 rows per CTA) at
 // 0.88 of the copy peak with whole rows and 0.94 with 3.5 KB pieces, while
 // pieces of 2 KB lost up to 12 % on the large batches.
+#ifndef MOE_PERMUTE_L2_EVICT_FIRST
+#define MOE_PERMUTE_L2_EVICT_FIRST 1
+#endif
+// CTAs of the dynamic kernel per SM (fewer if fewer fit).  Measured on
+// GB300 with the same ring: 4 per SM beat 5 on every workload (decode
+// permute 120.3 -> 116.5 us, skewed 324.5 -> 317.4, round-trip 1375.6 ->
+// 1364.1) and 3 beat 4 by up to 1 % (prefill fp8 344.0 -> 340.5 us, decode
+// unchanged); the L2 policy alone moved them by 0.2-0.4 %.
+#ifndef MOE_PERMUTE_DYN_CTAS_PER_SM
+#define MOE_PERMUTE_DYN_CTAS_PER_SM 3
+#endif
+#ifndef MOE_PERMUTE_DYN_MIN_BLOCKS
+#define MOE_PERMUTE_DYN_MIN_BLOCKS MOE_PERMUTE_DYN_CTAS_PER_SM
+#endif
 constexpr int kMinUnitBytes = MOE_PERMUTE_MIN_UNIT_BYTES;
 constexpr int kUnitsPerCta = MOE_PERMUTE_UNITS_PER_CTA;
 static_assert(kMinUnitBytes >= 16 && kMinUnitBytes % 16 == 0, "piece size");
+
+// Bulk store of receive rows, which nothing in the permute reads again: with
+// an evict-first L2 policy their lines go first when L2 needs room.
+__device__ __forceinline__ uint64_t store_policy() {
+  return MOE_PERMUTE_L2_EVICT_FIRST ? ptx::l2_evict_first_policy() : 0;
+}
+__device__ __forceinline__ void store_rows(void* dst, const void* src, uint32_t bytes, uint64_t policy) {
+  if (MOE_PERMUTE_L2_EVICT_FIRST)
+    ptx::bulk_s2g_hint(dst, src, bytes, policy);
+  else
+    ptx::bulk_s2g(dst, src, bytes);
+}
 
 __device__ __forceinline__ int warp_inclusive_scan(int v, int lane) {
 #pragma unroll
@@ -258,6 +284,7 @@ __global__ void __launch_bounds__(kPermuteThreads)
     int issued = prologue;
     int u = 0;
     bool ok = true;
+    const uint64_t policy = store_policy();
     for (; u < units; ++u) {
       const int s = u % S;
       if (!ptx::mbar_wait_parity_bounded(&full_bar[s], (u / S) & 1, kWaitLimitNs)) {
@@ -270,7 +297,7 @@ __global__ void __launch_bounds__(kPermuteThreads)
       const uint8_t* src = ring + static_cast<size_t>(s) * chunk;
       for (int k = 0; k < K; ++k) {
         const int32_t slot = sl[k];
-        if (slot >= 0) ptx::bulk_s2g(a.recv_x + slot * rb + static_cast<int64_t>(c) * chunk, src, bytes);
+        if (slot >= 0) store_rows(a.recv_x + slot * rb + static_cast<int64_t>(c) * chunk, src, bytes, policy);
       }
       ptx::bulk_commit();
       if (u + S < units) {
@@ -365,7 +392,7 @@ struct DynPlan {
   size_t off_padpre, smem;
 };
 
-__global__ void __launch_bounds__(kPermuteThreads)
+__global__ void __launch_bounds__(kPermuteThreads, MOE_PERMUTE_DYN_MIN_BLOCKS)
     permute_dyn_kernel(const PermuteArgs a, const DynPlan p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages];
@@ -491,6 +518,7 @@ __global__ void __launch_bounds__(kPermuteThreads)
   };
   int64_t j = 0;
   bool ok = true;
+  const uint64_t policy = store_policy();
   for (; j < issued; ++j) {
     const int s = static_cast<int>(j % S);
     if (!ptx::mbar_wait_parity_bounded(&full_bar[s], static_cast<uint32_t>((j / S) & 1), kWaitLimitNs)) {
@@ -512,9 +540,9 @@ __global__ void __launch_bounds__(kPermuteThreads)
         if (off == 0) set_error(a.err, MOE_ERR_CAPACITY);
         continue;
       }
-      ptx::bulk_s2g(a.recv_x + slot * rb + off, st, len);
+      store_rows(a.recv_x + slot * rb + off, st, len, policy);
       if (with_sf)
-        ptx::bulk_s2g(a.recv_sf + slot * srb, st + p.unit_bytes + p.slot_win, static_cast<uint32_t>(srb));
+        store_rows(a.recv_sf + slot * srb, st + p.unit_bytes + p.slot_win, static_cast<uint32_t>(srb), policy);
     }
     ptx::bulk_commit();
     if (!exhausted) {
@@ -603,12 +631,16 @@ int dyn_ctas_per_sm(size_t smem) {
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t stream) {
   if (dyn_applicable(a)) {
     DynPlan p = make_dyn_plan(a, 1);
-    int64_t resident = static_cast<int64_t>(dyn_ctas_per_sm(p.smem)) * device_sm_count();
+    auto ctas_per_sm = [](size_t smem) {
+      const int occ = dyn_ctas_per_sm(smem);
+      return MOE_PERMUTE_DYN_CTAS_PER_SM > 0 && MOE_PERMUTE_DYN_CTAS_PER_SM < occ ? MOE_PERMUTE_DYN_CTAS_PER_SM : occ;
+    };
+    int64_t resident = static_cast<int64_t>(ctas_per_sm(p.smem)) * device_sm_count();
     const int64_t want = ceil_div64(kUnitsPerCta * resident, max64(1, a.num_tokens));
     const int pieces = static_cast<int>(min64(want, max_pieces(a)));
     if (pieces > 1) {
       p = make_dyn_plan(a, pieces);
-      resident = static_cast<int64_t>(dyn_ctas_per_sm(p.smem)) * device_sm_count();
+      resident = static_cast<int64_t>(ctas_per_sm(p.smem)) * device_sm_count();
     }
     cudaError_t st = cudaFuncSetAttribute(permute_dyn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           static_cast<int>(p.smem));
