@@ -27,16 +27,24 @@
 namespace moe {
 namespace {
 
-// Grid = this many full waves at the kernel's occupancy (a grid of 1.7 waves
-// left a third of the SMs idle during the partial second wave).
+// Grid = whole waves at the kernel's occupancy, tokens shared out evenly over
+// exactly that many CTAs (a grid of 1.7 waves left a third of the SMs idle
+// during the partial second wave).  Small batches get more, smaller CTAs for
+// the block scheduler to balance: measured on GB300, 4 waves took decode's
+// combine from 90.5 to 88.2 us, while 131072 tokens ran 1 % faster with 2.
 #ifndef MOE_COMBINE_WAVES
 #define MOE_COMBINE_WAVES 2
+#endif
+#ifndef MOE_COMBINE_SMALL_WAVES
+#define MOE_COMBINE_SMALL_WAVES 4
+#endif
+#ifndef MOE_COMBINE_SMALL_TOKENS_PER_CTA
+#define MOE_COMBINE_SMALL_TOKENS_PER_CTA 8   // "small": fewer tokens per CTA than this at SMALL_WAVES
 #endif
 
 constexpr int kCombineThreads = 256;
 constexpr int kKGroup = 8;              // expert rows loaded before their FMAs
 constexpr int kMaxTokensPerCta = 64;
-constexpr int kWaves = MOE_COMBINE_WAVES;
 #ifndef MOE_COMBINE_VEC_UNROLL
 #define MOE_COMBINE_VEC_UNROLL 1
 #endif
@@ -56,15 +64,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
+// CTA b's share of n items split over g CTAs: [share_start(b), share_start(b + 1)).
+__device__ __forceinline__ int64_t share_start(int64_t b, int64_t n, int64_t g) {
+  return b * (n / g) + min64(b, n % g);
+}
+
 __global__ void __launch_bounds__(kCombineThreads)
-    combine_kernel(const CombineArgs a, int tokens_per_cta) {
+    combine_kernel(const CombineArgs a, int max_tokens) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int K = a.topk;
   int32_t* slot_s = reinterpret_cast<int32_t*>(smem);
-  float* w_s = reinterpret_cast<float*>(smem + sizeof(int32_t) * tokens_per_cta * K);
+  float* w_s = reinterpret_cast<float*>(smem + sizeof(int32_t) * max_tokens * K);
 
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * tokens_per_cta;
-  const int ntok = static_cast<int>(max64(0, min64(tokens_per_cta, a.num_tokens - t0)));
+  const int64_t t0 = share_start(blockIdx.x, a.num_tokens, gridDim.x);
+  const int ntok = static_cast<int>(share_start(static_cast<int64_t>(blockIdx.x) + 1, a.num_tokens, gridDim.x) - t0);
   ptx::grid_dependency_wait();
   ptx::grid_dependency_launch_dependents();
   // Slots and weights of the CTA's tokens; kBatch independent loads of each per thread.
@@ -161,14 +174,17 @@ int combine_ctas_per_sm() {
 }  // namespace
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
-  const int sms = device_sm_count();
-  const int64_t target_ctas = static_cast<int64_t>(kWaves) * combine_ctas_per_sm() * sms;
-  int64_t tpc = ceil_div64(max64(a.num_tokens, 1), target_ctas);
-  tpc = max64(1, min64(tpc, kMaxTokensPerCta));
-  const int64_t grid = max64(1, ceil_div64(a.num_tokens, tpc));
-  const size_t smem = (sizeof(int32_t) + sizeof(float)) * static_cast<size_t>(tpc) * a.topk;
+  const int64_t resident = static_cast<int64_t>(combine_ctas_per_sm()) * device_sm_count();
+  const bool small = a.num_tokens < static_cast<int64_t>(MOE_COMBINE_SMALL_TOKENS_PER_CTA) * MOE_COMBINE_SMALL_WAVES * resident;
+  // Whole waves, each CTA at least one token and at most kMaxTokensPerCta
+  // (shared out evenly: counts differ by at most one).
+  int64_t grid = (small ? MOE_COMBINE_SMALL_WAVES : MOE_COMBINE_WAVES) * resident;
+  grid = max64(grid, ceil_div64(a.num_tokens, kMaxTokensPerCta));
+  grid = max64(1, min64(grid, a.num_tokens));
+  const int64_t max_tokens = max64(1, ceil_div64(a.num_tokens, grid));
+  const size_t smem = (sizeof(int32_t) + sizeof(float)) * static_cast<size_t>(max_tokens) * a.topk;
   const cudaError_t st = launch_pdl(combine_kernel, dim3(static_cast<unsigned>(grid)), dim3(kCombineThreads), smem,
-                                    stream, a, static_cast<int>(tpc));
+                                    stream, a, static_cast<int>(max_tokens));
   if (st != cudaSuccess) return st;
   count_launch();
   return cudaSuccess;
