@@ -30,7 +30,12 @@ ERROR_NAMES = {
 
 class LayoutError(RuntimeError):
     def __init__(self, what: str, status: int):
-        super().__init__(f"{what}: {ERROR_NAMES.get(status, status)} ({strerror(status)})")
+        text = f"{what}: {ERROR_NAMES.get(status, status)} ({strerror(status)})"
+        if status == 2:   # MOE_ERR_CUDA: add the CUDA error behind it
+            msg = ctypes.c_char_p()
+            code = load_library().moe_last_cuda_error(ctypes.byref(msg))
+            text += f"; CUDA error {code}: {msg.value.decode() if msg.value else '?'}"
+        super().__init__(text)
         self.status = status
 
 
@@ -88,6 +93,8 @@ def load_library() -> ctypes.CDLL:
         lib.moe_strerror.restype = ctypes.c_char_p
         lib.moe_kernel_launches.argtypes = []
         lib.moe_kernel_launches.restype = ctypes.c_uint64
+        lib.moe_last_cuda_error.argtypes = [ctypes.POINTER(ctypes.c_char_p)]
+        lib.moe_last_cuda_error.restype = ctypes.c_int
         for name in ("moe_layout_workspace_bytes", "moe_layout_count", "moe_layout_scan", "moe_layout_build",
                      "moe_layout_build_i32",
                      "moe_layout_rank_rows", "moe_dispatch_permute_ranks", "moe_dispatch_from_host",

@@ -56,7 +56,13 @@ int check_workspace(const moe_layout_desc* d, const void* ws, size_t ws_bytes, W
   return MOE_OK;
 }
 
-int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+thread_local int t_last_cuda_error = 0;
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  t_last_cuda_error = static_cast<int>(e);
+  return MOE_ERR_CUDA;
+}
 
 template <typename T>
 T* at(void* ws, size_t off) {
@@ -321,5 +327,10 @@ const char* moe_strerror(int status) {
 }
 
 uint64_t moe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int moe_last_cuda_error(const char** message) {
+  if (message != nullptr) *message = cudaGetErrorString(static_cast<cudaError_t>(t_last_cuda_error));
+  return t_last_cuda_error;
+}
 
 }  // extern "C"

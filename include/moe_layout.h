@@ -347,6 +347,13 @@ MOE_API const char* moe_strerror(int status);
 /* Number of kernels this library has launched in this process so far. */
 MOE_API uint64_t moe_kernel_launches(void);
 
+/*
+ * The CUDA error code (cudaError_t) behind this thread's most recent
+ * MOE_ERR_CUDA, or 0 if there was none; *message (if non-NULL) receives its
+ * description.  Diagnostics only: a status the pages do not define.
+ */
+MOE_API int moe_last_cuda_error(const char** message);
+
 #ifdef __cplusplus
 }
 #endif

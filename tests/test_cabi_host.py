@@ -98,6 +98,15 @@ def test_host_checks_reject_before_launch(lib):
     assert lib.moe_layout_get_error(None, None, None) == 1
 
 
+def test_last_cuda_error_is_readable_without_a_gpu(lib):
+    lib.moe_last_cuda_error.argtypes = [ctypes.POINTER(ctypes.c_char_p)]
+    lib.moe_last_cuda_error.restype = ctypes.c_int
+    msg = ctypes.c_char_p()
+    assert lib.moe_last_cuda_error(ctypes.byref(msg)) == 0      # no CUDA call has failed in this thread
+    assert msg.value
+    assert lib.moe_last_cuda_error(None) == 0
+
+
 def test_strerror_and_launch_counter(lib):
     for code, name in binding.ERROR_NAMES.items():
         assert lib.moe_strerror(code)
