@@ -41,7 +41,7 @@ L2_FLUSH_BYTES = 256 << 20          # > 2x the 129 MB L2
 # DRAM traffic of the permute kernel from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), per launch, scaled to the decode workload, tied to
 # the kernel sources it was measured on.  bench reports null if they changed.
-PERMUTE_TRAFFIC = {"sha256": "0efef350c87eaeede7a793591d2220baf5a66b545748de0f9b43e958cea03f58",
+PERMUTE_TRAFFIC = {"sha256": "cea36703da7e5e30e037cb7205f4bb423a47dafd0f9701c8abdca070a12f6d98",
                    "workload": "decode", "bytes_per_launch": 58_910_208 + 647_979_776}
 PERMUTE_SOURCES = ["counting_sort_bucketization_gb300/csrc/permute_kernel.cu",
                    "counting_sort_bucketization_gb300/csrc/ptx.cuh",

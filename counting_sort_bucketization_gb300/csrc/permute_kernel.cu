@@ -18,13 +18,15 @@
 //    stores; gap rows are split evenly over CTAs by a prefix sum of gap sizes.
 //
 // Two kernels:
-//  - permute_dyn_kernel (the default): a persistent grid, one wave at the
-//    occupancy the shared-memory ring allows, whose TMA threads claim tokens
-//    one at a time from a counter in the workspace.  A measured trace of the
+//  - permute_dyn_kernel (the default): a persistent grid of one wave (3 CTAs
+//    per SM) whose TMA threads claim units -- pieces of token rows -- one at
+//    a time from a counter in the workspace.  A measured trace of the
 //    statically split kernel showed SMs with equal shares finishing as much
 //    as 40 % apart, and a grid of 1.3 waves when rows are small; claiming
-//    tokens keeps every SM busy to the end.  The token's slots and its scale
-//    factors come in by bulk copy on the same mbarrier as its row.
+//    keeps every SM busy to the end, and cutting rows into pieces when a CTA
+//    would see few rows keeps most units in the counter instead of in the
+//    CTAs' rings.  A unit's slots and (with the row's first piece) its scale
+//    factors come in by bulk copy on the same mbarrier as its bytes.
 //  - permute_kernel: a static split of contiguous token blocks, used when a
 //    row is wider than one 16 KiB slice or scale rows are not 16-byte sized.
 #include <cuda_runtime.h>
