@@ -382,13 +382,13 @@ def run_native(args, rank, world, local):
     h2d = idx_h.numel() * 8 + x_h.numel() * x_h.element_size() + wt_h.numel() * 4 + \
         (sf_h.numel() * 4 if sf_h is not None else 0)
     d2h = outs_h[0].numel() * outs_h[0].element_size()
-    chunk = -(-N // max(1, args.e2e_chunks))
+    chunk_of = lambda n_chunks: -(-N // max(1, n_chunks))
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
     expert = (lambda lay_, recv_, recv_sf_: eo) if do_combine else None
 
-    def e2e_ms_per_step(n_lanes):
+    def e2e_ms_per_step(n_lanes, n_chunks):
         pipe = binding.HostPipeline(w, cap, H, x_dtype=x_d.dtype, sf_cols=sf_d.shape[1] if sf_d is not None else 0,
-                                    lanes=n_lanes, chunk_tokens=chunk, device=dev)
+                                    lanes=n_lanes, chunk_tokens=chunk_of(n_chunks), device=dev)
         for i in range(2 * n_lanes):
             pipe.submit(idx_h, x_h, wt_h, outs_h[i % n_lanes], expert, sf_h)
         pipe.join(stream)
@@ -403,8 +403,9 @@ def run_native(args, rank, world, local):
         assert pipe.errors() == [0] * n_lanes, "device error in the end-to-end steps"
         return a.elapsed_time(b) / e2e_steps
 
-    e2e_step_ms = reduce_max(e2e_ms_per_step(lanes), world, dev)
-    e2e_one_ms = reduce_max(e2e_ms_per_step(1), world, dev) if lanes > 1 else e2e_step_ms
+    e2e_step_ms = reduce_max(e2e_ms_per_step(lanes, args.e2e_chunks), world, dev)
+    # One batch in flight, its copies overlapped with the kernels in 4 chunks: the reference point.
+    e2e_one_ms = reduce_max(e2e_ms_per_step(1, 4), world, dev)
 
     if rank != 0:
         return
@@ -431,7 +432,7 @@ def run_native(args, rank, world, local):
         "layout": {"valid_pairs": ab["P"], "rows": ab["rows"], "tokens_routed": ab["tokens_routed"]},
         "e2e": {"value": world * N / (e2e_step_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps, "chunks": args.e2e_chunks,
-                "batches_in_flight": lanes, "value_one_batch_in_flight": world * N / (e2e_one_ms / 1e3),
+                "batches_in_flight": lanes, "value_one_batch_in_flight_4_chunks": world * N / (e2e_one_ms / 1e3),
                 "api": "HostPipeline: moe_dispatch_from_host + moe_combine_to_host" if do_combine
                 else "HostPipeline: moe_dispatch_from_host + receive rows copied back"},
         "gpu_launches": launches,
@@ -498,7 +499,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=list(wl.WORKLOADS), default="decode")
     ap.add_argument("--e2e-steps", type=int, default=50)
-    ap.add_argument("--e2e-chunks", type=int, default=2, help="token chunks the host copies are split into")
+    ap.add_argument("--e2e-chunks", type=int, default=1, help="token chunks the host copies are split into")
     ap.add_argument("--e2e-lanes", type=int, default=3, help="batches in flight in the end-to-end leg")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-max-passes", type=int, default=20)
