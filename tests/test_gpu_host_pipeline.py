@@ -121,3 +121,29 @@ def test_pipelined_batches(name, chunk, lanes):
     assert pipe.errors() == [0] * lanes
     for b, o in zip(batches, outs):
         np.testing.assert_array_equal(o.view(torch.int16).numpy().view(np.uint16), oracle_batch(b, w))
+
+
+def test_pipelined_dispatch_only_fp8():
+    # expert=None: the receive rows come back to host memory; fp8 rows with scale factors
+    w = wl.WORKLOADS["prefill_fp8"].replace(num_tokens=2000)
+    cap = wl.worst_case_rows(w)
+    pipe = binding.HostPipeline(w, cap, w.hidden, x_dtype=torch.float8_e4m3fn, sf_cols=w.hidden // w.sf_block,
+                                lanes=2, chunk_tokens=700, device=DEV)
+    batches = [wl.make(w, 40 + b) for b in range(3)]
+    outs = [torch.zeros((cap, w.hidden), dtype=torch.uint8).pin_memory().view(torch.float8_e4m3fn) for _ in batches]
+    done = []
+    for b, o in zip(batches, outs):
+        done.append(pipe.submit(b["topk_idx"].pin_memory(), b["x"].pin_memory(), b["weights"].pin_memory(), o, None,
+                                sf_host=b["sf"].pin_memory()))
+    for ev in done:
+        ev.synchronize()
+    assert pipe.errors() == [0, 0]
+    for i, (b, o) in enumerate(zip(batches, outs)):
+        ref = oracle.layout(b["topk_idx"].numpy(), w.num_experts, w.num_ranks, w.alignment)
+        rows = ref["total_rows"]
+        _, want, want_sf = oracle.permute(u8(b["x"]), ref["dst_slot"], ref["expert_offset"], ref["expert_count"],
+                                          rows, sf_bytes=u8(b["sf"]))
+        np.testing.assert_array_equal(u8(o[:rows]), want)
+        if i == len(batches) - 1:   # the lane of the last batch still holds its scale rows
+            lane = pipe.lane(i % pipe.lanes)
+            np.testing.assert_array_equal(u8(lane["recv_sf"][:rows]), want_sf)
