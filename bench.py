@@ -41,8 +41,8 @@ L2_FLUSH_BYTES = 256 << 20          # > 2x the 129 MB L2
 # DRAM traffic of the permute kernel from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), per launch, scaled to the decode workload, tied to
 # the kernel sources it was measured on.  bench reports null if they changed.
-PERMUTE_TRAFFIC = {"sha256": "cea36703da7e5e30e037cb7205f4bb423a47dafd0f9701c8abdca070a12f6d98",
-                   "workload": "decode", "bytes_per_launch": 58_910_208 + 647_979_776}
+PERMUTE_TRAFFIC = {"sha256": "801a87ccc6e447dd9c90ba6f0fdab434053020367ab93c5a23a974ccef11147e",
+                   "workload": "decode", "bytes_per_launch": 58_918_144 + 647_613_696}
 PERMUTE_SOURCES = ["counting_sort_bucketization_gb300/csrc/permute_kernel.cu",
                    "counting_sort_bucketization_gb300/csrc/ptx.cuh",
                    "counting_sort_bucketization_gb300/csrc/common.cuh"]

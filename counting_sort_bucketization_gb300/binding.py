@@ -323,7 +323,10 @@ def _stream_ptr(s) -> ctypes.c_void_p:
 
 def dispatch_from_host(lay: "Layout", topk_idx_host, x_host, topk_idx, x, recv_x, weights_host=None, weights=None,
                        sf_host=None, sf=None, recv_sf=None, chunk_tokens=0, stream=None, copy_stream=None) -> None:
-    """Host ids/rows in, layout + permuted rows on the device; copies overlapped with the permute."""
+    """Host ids/rows in, layout + permuted rows on the device; copies overlapped with the permute.
+
+    Asynchronous: the host tensors must stay alive and unwritten until
+    ``stream`` reaches this point (the copies run outside torch's caching)."""
     d = lay.desc
     N, K = int(d.num_tokens), int(d.topk)
     s = stream if stream is not None else torch.cuda.current_stream()
@@ -346,7 +349,9 @@ def dispatch_from_host(lay: "Layout", topk_idx_host, x_host, topk_idx, x, recv_x
 
 def combine_to_host(lay: "Layout", expert_out, weights, out, out_host, chunk_tokens=0, stream=None,
                     copy_stream=None) -> None:
-    """Combine on the device with each chunk's result copied to ``out_host`` while the next is combined."""
+    """Combine on the device with each chunk's result copied to ``out_host`` while the next is combined.
+
+    Asynchronous: ``out_host`` must stay alive and unread until ``stream`` reaches this point."""
     d = lay.desc
     N, K = int(d.num_tokens), int(d.topk)
     s = stream if stream is not None else torch.cuda.current_stream()
@@ -455,8 +460,11 @@ class HostPipeline:
     batch's copy back to the host overlaps the next batch's copy in: the host
     link carries both directions at once.  ``submit`` returns an event that
     completes when the batch's result is in ``out_host``; until then the
-    batch's host buffers must stay untouched.  A lane is reused only after
-    its previous batch, by stream order.
+    batch's host buffers must not be written.  The pipeline keeps a reference
+    to them until then, so temporaries (``x.pin_memory()`` passed inline) are
+    safe: the copies run outside torch, which would otherwise hand a freed
+    page-locked block to the next allocation while a copy still reads it.  A
+    lane is reused only after its previous batch, by stream order.
     """
 
     def __init__(self, desc, capacity_rows: int, hidden: int, x_dtype=torch.bfloat16, sf_cols: int = 0,
@@ -482,6 +490,7 @@ class HostPipeline:
             }
             self._lanes.append(lane)
         self._next = 0
+        self._in_flight = []   # (event, host tensors) of batches not known to be done
 
     @property
     def lanes(self) -> int:
@@ -513,6 +522,8 @@ class HostPipeline:
                             stream=s, copy_stream=cs)
         done = torch.cuda.Event()
         done.record(s)
+        self._in_flight = [(ev, refs) for ev, refs in self._in_flight if not ev.query()]
+        self._in_flight.append((done, (topk_idx_host, x_host, weights_host, out_host, sf_host)))
         return done
 
     def join(self, stream=None) -> None:
