@@ -422,7 +422,10 @@ def run_native(args, rank, world, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(w),
         "roofline": {"kernel": "permute_dyn_kernel", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "peak_source": peaks["source"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": traffic, "algorithmic_bytes_per_launch": ab["permute"]},
+                     "traffic": traffic, "algorithmic_bytes_per_launch": ab["permute"],
+                     "note": "algorithmic bytes include the launch's last writes, still dirty in L2 when it "
+                             "ends (written back during the next kernel): frac can read a little above 1 and "
+                             "traffic below the algorithmic bytes"},
         "kernels_ms": {"layout": kern_ms["layout"], "permute": kern_ms["permute"],
                        "sf_col_major": kern_ms.get("sf_col_major"), "combine": kern_ms.get("combine")},
         "kernels_gbs": {"permute": ab["permute"] / permute_s / 1e9,
