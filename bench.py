@@ -41,8 +41,8 @@ L2_FLUSH_BYTES = 256 << 20          # > 2x the 129 MB L2
 # DRAM traffic of the permute kernel from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), per launch, scaled to the decode workload, tied to
 # the kernel sources it was measured on.  bench reports null if they changed.
-PERMUTE_TRAFFIC = {"sha256": "801a87ccc6e447dd9c90ba6f0fdab434053020367ab93c5a23a974ccef11147e",
-                   "workload": "decode", "bytes_per_launch": 58_918_144 + 647_613_696}
+PERMUTE_TRAFFIC = {"sha256": "aec3d083b3d155727c4d5b98ff24141c40276ae1a6d61a68a82d7f2465491159",
+                   "workload": "decode", "bytes_per_launch": 58_907_648 + 646_813_440}
 PERMUTE_SOURCES = ["counting_sort_bucketization_gb300/csrc/permute_kernel.cu",
                    "counting_sort_bucketization_gb300/csrc/ptx.cuh",
                    "counting_sort_bucketization_gb300/csrc/common.cuh"]
@@ -248,11 +248,14 @@ def run_layout_only(args, local):
     torch.cuda.set_device(dev)
     w = wl.WORKLOADS[args.workload]
     idx = wl.draw_topk_idx(w, wl.SEEDS[w.name]).to(dev)
+    if args.ids_int32:
+        idx = idx.to(torch.int32)
     lay = binding.Layout(w, wl.worst_case_rows(w), device=dev)
     flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     times = {}
-    for fused in (True, False):
+    # The two-call API (count, then scan) takes int64 ids only.
+    for fused in ((True,) if args.ids_int32 else (True, False)):
         evs = []
         for i in range(args.warmup + args.steps):
             flush_w.zero_()
@@ -266,7 +269,9 @@ def run_layout_only(args, local):
         torch.cuda.synchronize(dev)
         times["one_call" if fused else "two_calls"] = float(np.mean([a.elapsed_time(b) for a, b in evs]))
     assert lay.error() == 0
-    print(json.dumps({"mode": "layout-only", "config": config_of(w), "steps": args.steps, "warmup": args.warmup,
+    cfg = config_of(w)
+    cfg["ids"] = "int32" if args.ids_int32 else "int64"
+    print(json.dumps({"mode": "layout-only", "config": cfg, "steps": args.steps, "warmup": args.warmup,
                       "layout_ms": times, "tokens_per_s": {k: w.num_tokens / (v / 1e3) for k, v in times.items()}}),
           flush=True)
 
@@ -308,6 +313,15 @@ def run_native(args, rank, world, local):
         row_e = torch.searchsorted(off[1:], torch.arange(rows, device=dev), right=True)
         eo[:rows] = (recv[:rows].float() * inp["expert_scale"].to(dev)[row_e][:, None]).to(torch.bfloat16)
     assert lay.error() == 0, "device error during set-up"
+    # Non-expand mode: one row per (token, rank reached), rank-contiguous, no padding.
+    ne = args.non_expand
+    if ne:
+        ne_cap = N * w.num_ranks
+        lay.rank_rows(idx_d, capacity_rows=ne_cap)
+        recv_ne = torch.empty((ne_cap, H), dtype=x_d.dtype, device=dev)
+        recv_ne_sf = torch.empty((ne_cap, sf_d.shape[1]), dtype=sf_d.dtype, device=dev) if sf_d is not None else None
+        lay.permute_ranks(x_d, recv_ne, sf_d, recv_ne_sf)
+        assert lay.error() == 0, "device error during set-up"
     flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
 
@@ -317,12 +331,16 @@ def run_native(args, rank, world, local):
 
     # The step's kernels in order, one event after each (and one before the
     # first): every timed interval holds exactly one step of the path.
-    stages = [("layout", lambda: lay.build(idx_d)),
-              ("permute", lambda: lay.permute(x_d, recv, perm_sf, perm_recv_sf))]
-    if sf_cm:
-        stages.append(("sf_col_major", lambda: lay.permute_sf_col_major(sf_d, recv_sf_cm)))
-    if do_combine:
-        stages.append(("combine", lambda: lay.combine(eo, wt_d, out)))
+    stages = [("layout", lambda: lay.build(idx_d))]
+    if ne:
+        stages += [("rank_rows", lambda: lay.rank_rows(idx_d, capacity_rows=ne_cap)),
+                   ("permute_ranks", lambda: lay.permute_ranks(x_d, recv_ne, sf_d, recv_ne_sf))]
+    else:
+        stages.append(("permute", lambda: lay.permute(x_d, recv, perm_sf, perm_recv_sf)))
+        if sf_cm:
+            stages.append(("sf_col_major", lambda: lay.permute_sf_col_major(sf_d, recv_sf_cm)))
+        if do_combine:
+            stages.append(("combine", lambda: lay.combine(eo, wt_d, out)))
 
     def step(ev):
         ev[0].record(stream)
@@ -362,8 +380,14 @@ def run_native(args, rank, world, local):
     ms_per_step = reduce_max(float(step_ms.mean()), world, dev)
     kern_ms = dict(zip([name for name, _ in stages], per.mean(axis=0).tolist()))
     ab = algorithmic_bytes(w, lay, sf_cm)
+    if ne:
+        # each routed token's row read once, one row written per (token, rank reached), the slots read
+        rows_ne = int(lay.rank_psum[-1].item())
+        rb_all = w.row_bytes + w.sf_row_bytes
+        ab["permute_ranks"] = ab["tokens_routed"] * rb_all + rows_ne * rb_all + N * w.topk * 4
+        ab["rows_non_expand"] = rows_ne
     value = world * N / (ms_per_step / 1e3)
-    dispatch_ms = kern_ms["layout"] + kern_ms["permute"] + kern_ms.get("sf_col_major", 0.0)
+    dispatch_ms = sum(v for k, v in kern_ms.items() if k != "combine")
 
     # End to end through the public API with host buffers: pinned ids, rows
     # and weights in, the combined tokens back (dispatch-only workloads: the
@@ -383,6 +407,7 @@ def run_native(args, rank, world, local):
         (sf_h.numel() * 4 if sf_h is not None else 0)
     d2h = outs_h[0].numel() * outs_h[0].element_size()
     chunk_of = lambda n_chunks: -(-N // max(1, n_chunks))
+    e2e_line = None
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
     expert = (lambda lay_, recv_, recv_sf_: eo) if do_combine else None
 
@@ -403,17 +428,25 @@ def run_native(args, rank, world, local):
         assert pipe.errors() == [0] * n_lanes, "device error in the end-to-end steps"
         return a.elapsed_time(b) / e2e_steps
 
-    e2e_step_ms = reduce_max(e2e_ms_per_step(lanes, args.e2e_chunks), world, dev)
-    # One batch in flight, its copies overlapped with the kernels in 4 chunks: the reference point.
-    e2e_one_ms = reduce_max(e2e_ms_per_step(1, 4), world, dev)
+    if not ne:   # the end-to-end leg is the expand path's
+        e2e_step_ms = reduce_max(e2e_ms_per_step(lanes, args.e2e_chunks), world, dev)
+        # One batch in flight, its copies overlapped with the kernels in 4 chunks: the reference point.
+        e2e_one_ms = reduce_max(e2e_ms_per_step(1, 4), world, dev)
+        e2e_line = {"value": world * N / (e2e_step_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps, "chunks": args.e2e_chunks,
+                    "batches_in_flight": lanes,
+                    "value_one_batch_in_flight_4_chunks": world * N / (e2e_one_ms / 1e3),
+                    "api": "HostPipeline: moe_dispatch_from_host + moe_combine_to_host" if do_combine
+                    else "HostPipeline: moe_dispatch_from_host + receive rows copied back"}
 
     if rank != 0:
         return
     peaks = measured_peaks()
-    permute_s = kern_ms["permute"] / 1e3
-    achieved = ab["permute"] / permute_s / 1e9
+    dom = "permute_ranks" if ne else "permute"
+    permute_s = kern_ms[dom] / 1e3
+    achieved = ab[dom] / permute_s / 1e9
     traffic = None
-    if PERMUTE_TRAFFIC and PERMUTE_TRAFFIC.get("sha256") == sources_sha256(PERMUTE_SOURCES) \
+    if not ne and PERMUTE_TRAFFIC and PERMUTE_TRAFFIC.get("sha256") == sources_sha256(PERMUTE_SOURCES) \
             and PERMUTE_TRAFFIC.get("workload") == w.name:
         traffic = PERMUTE_TRAFFIC["bytes_per_launch"]
     line = {
@@ -422,30 +455,31 @@ def run_native(args, rank, world, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(w),
         "roofline": {"kernel": "permute_dyn_kernel", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "peak_source": peaks["source"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": traffic, "algorithmic_bytes_per_launch": ab["permute"],
+                     "traffic": traffic, "algorithmic_bytes_per_launch": ab[dom],
                      "note": "algorithmic bytes include the launch's last writes, still dirty in L2 when it "
                              "ends (written back during the next kernel): frac can read a little above 1 and "
                              "traffic below the algorithmic bytes"},
-        "kernels_ms": {"layout": kern_ms["layout"], "permute": kern_ms["permute"],
-                       "sf_col_major": kern_ms.get("sf_col_major"), "combine": kern_ms.get("combine")},
-        "kernels_gbs": {"permute": ab["permute"] / permute_s / 1e9,
-                        "sf_col_major": (ab["sf_col_major"] / (kern_ms["sf_col_major"] / 1e3) / 1e9) if sf_cm else None,
-                        "combine": (ab["combine"] / (kern_ms["combine"] / 1e3) / 1e9) if do_combine else None},
+        "kernels_ms": dict(kern_ms) if ne else {
+            "layout": kern_ms["layout"], "permute": kern_ms["permute"],
+            "sf_col_major": kern_ms.get("sf_col_major"), "combine": kern_ms.get("combine")},
+        "kernels_gbs": {"permute_ranks": achieved} if ne else {
+            "permute": ab["permute"] / permute_s / 1e9,
+            "sf_col_major": (ab["sf_col_major"] / (kern_ms["sf_col_major"] / 1e3) / 1e9) if sf_cm else None,
+            "combine": (ab["combine"] / (kern_ms["combine"] / 1e3) / 1e9) if do_combine else None},
         "dispatch_tokens_per_s": world * N / (dispatch_ms / 1e3),
         "layout": {"valid_pairs": ab["P"], "rows": ab["rows"], "tokens_routed": ab["tokens_routed"]},
-        "e2e": {"value": world * N / (e2e_step_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps, "chunks": args.e2e_chunks,
-                "batches_in_flight": lanes, "value_one_batch_in_flight_4_chunks": world * N / (e2e_one_ms / 1e3),
-                "api": "HostPipeline: moe_dispatch_from_host + moe_combine_to_host" if do_combine
-                else "HostPipeline: moe_dispatch_from_host + receive rows copied back"},
+        "e2e": e2e_line,
         "gpu_launches": launches,
         "wall_s_timed_region": t_wall,
         "clocks": sampler.summary() if sampler else None,
     }
+    if ne:
+        line["config"]["layout_mode"] = "non-expand: one row per (token, rank reached), rank-contiguous, no padding"
+        line["layout"]["rows_non_expand"] = ab["rows_non_expand"]
     if sf_d is not None:
         line["config"]["sf_layout"] = ("column-major, ld = capacity rounded up to 4 words (e2e leg: row-major)"
                                        if sf_cm else "row-major, moved by the permute")
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not ne:
         runner = OracleRunner(w, inp)
         tps, passes = runner.time_passes(args.cpu_seconds, args.cpu_max_passes)
         line["cpu_baseline"] = {"value": tps, "unit": UNIT, "cores": 1, "kind": "oracle",
@@ -511,6 +545,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--sf-col-major", action="store_true",
                     help="fp8 workloads: scale factors column-major (TMA-aligned) by their own kernel")
+    ap.add_argument("--ids-int32", action="store_true", help="--layout-only: int32 routing ids")
+    ap.add_argument("--non-expand", action="store_true",
+                    help="time the non-expand layout instead: layout, rank rows, rank-contiguous permute")
     ap.add_argument("--layout-only", action="store_true",
                     help="time only the layout step (count, scan, maps) on the chosen workload")
     return ap.parse_args(argv)

@@ -423,8 +423,9 @@ class Layout:
         N, K, R = int(self.desc.num_tokens), int(self.desc.topk), int(self.desc.num_ranks)
         cap = N * R if capacity_rows is None else int(capacity_rows)
         dev = self.dst_slot.device
-        self.rank_slot = torch.empty(max(N * K, 1), dtype=torch.int32, device=dev)
-        self.rank_src = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)[:cap]
+        if getattr(self, "rank_src", None) is None or self.rank_src.numel() != cap:   # reuse across calls
+            self.rank_slot = torch.empty(max(N * K, 1), dtype=torch.int32, device=dev)
+            self.rank_src = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)[:cap]
         layout_rank_rows(self.desc, topk_idx, self.rank_count, self.workspace, self.rank_slot, self.rank_src,
                          stream)
         return self

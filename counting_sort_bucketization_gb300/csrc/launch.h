@@ -61,6 +61,7 @@ struct PermuteArgs {
   int zero_pad;
   int* err;
   unsigned* work;                // [2] token counter + finished-CTA counter (zero between launches)
+  bool non_expand;               // rows of the non-expand layout (sizes the dynamic kernel's pieces)
 };
 
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t stream);

@@ -239,6 +239,7 @@ int moe_dispatch_permute_ranks(const moe_layout_desc* desc, const void* x, int64
   a.zero_pad = 0;
   a.err = at<int>(workspace, w.err_off);
   a.work = at<unsigned>(workspace, w.work_off);
+  a.non_expand = true;
   return cuda_status(launch_permute(a, static_cast<cudaStream_t>(stream)));
 }
 

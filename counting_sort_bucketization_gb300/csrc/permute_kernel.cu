@@ -68,6 +68,9 @@ constexpr int kSfRegWords = 4;  // scale-factor words a lane keeps in registers
 #ifndef MOE_PERMUTE_MIN_UNIT_BYTES
 #define MOE_PERMUTE_MIN_UNIT_BYTES 3584
 #endif
+#ifndef MOE_PERMUTE_RANKS_MIN_UNIT_BYTES
+#define MOE_PERMUTE_RANKS_MIN_UNIT_BYTES 7168
+#endif
 #ifndef MOE_PERMUTE_UNITS_PER_CTA
 #define MOE_PERMUTE_UNITS_PER_CTA 48
 #endif
@@ -75,7 +78,10 @@ constexpr int kSfRegWords = 4;  // scale-factor words a lane keeps in registers
 // least kUnitsPerCta units, but no piece below kMinUnitBytes: a sweep of
 // fixed piece sizes on GB300 put decode-sized batches (6-7 rows per CTA) at
 // 0.88 of the copy peak with whole rows and 0.94 with 3.5 KB pieces, while
-// pieces of 2 KB lost up to 12 % on the large batches.
+// pieces of 2 KB lost up to 12 % on the large batches.  The non-expand
+// permute (one row per token and rank reached: ~5 of 8 slots hold a row on
+// decode) wants larger pieces: 7 KB took its decode permute from 75.8 to
+// 61.1 us, 3.5 KB pieces being no better for its larger batches.
 #ifndef MOE_PERMUTE_L2_EVICT_FIRST
 #define MOE_PERMUTE_L2_EVICT_FIRST 1
 #endif
@@ -91,8 +97,10 @@ constexpr int kSfRegWords = 4;  // scale-factor words a lane keeps in registers
 #define MOE_PERMUTE_DYN_MIN_BLOCKS MOE_PERMUTE_DYN_CTAS_PER_SM
 #endif
 constexpr int kMinUnitBytes = MOE_PERMUTE_MIN_UNIT_BYTES;
+constexpr int kRanksMinUnitBytes = MOE_PERMUTE_RANKS_MIN_UNIT_BYTES;
 constexpr int kUnitsPerCta = MOE_PERMUTE_UNITS_PER_CTA;
 static_assert(kMinUnitBytes >= 16 && kMinUnitBytes % 16 == 0, "piece size");
+static_assert(kRanksMinUnitBytes >= 16 && kRanksMinUnitBytes % 16 == 0, "piece size");
 
 // Bulk store of receive rows, which nothing in the permute reads again: with
 // an evict-first L2 policy their lines go first when L2 needs room.
@@ -576,7 +584,10 @@ __global__ void __launch_bounds__(kPermuteThreads, MOE_PERMUTE_DYN_MIN_BLOCKS)
   }
 }
 
-int max_pieces(const PermuteArgs& a) { return static_cast<int>(max64(1, ceil_div64(a.row_bytes, kMinUnitBytes))); }
+int max_pieces(const PermuteArgs& a) {
+  const int min_unit = a.non_expand ? kRanksMinUnitBytes : kMinUnitBytes;
+  return static_cast<int>(max64(1, ceil_div64(a.row_bytes, min_unit)));
+}
 
 bool dyn_applicable(const PermuteArgs& a) {
   if (a.row_bytes > kMaxChunkBytes || a.work == nullptr) return false;
