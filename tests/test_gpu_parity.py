@@ -189,6 +189,7 @@ EDGE = [
     _w(5000, 8, 256, 8, 128, routing="zipf", zipf_s=2.5, mask_prob=0.1, H=32),  # extreme skew
     _w(40, 2, 8, 2, 4, H=8192 * 2),              # rows wider than one 16 KiB bulk slice
     _w(129, 8, 16, 4, 4, H=384, row_dtype="fp8"),  # fp8 rows, 12-byte scale-factor rows
+    _w(500, 4, 16, 4, 4096, H=16),               # alignment 4096: nearly every receive row is padding
     _w(1500, 8, 64, 8, 4, H=7168, row_dtype="fp8"),  # rows cut in 2 pieces, scale rows with the first
     _w(3000, 8, 64, 8, 16, H=5000),              # rows cut in 3 pieces, the last one shorter
     _w(40007, 3, 40, 5, 16, H=16),               # one-call layout in the cooperative kernel, ragged last tile
