@@ -342,20 +342,31 @@ def run_native(args, rank, world, local):
         if do_combine:
             stages.append(("combine", lambda: lay.combine(eo, wt_d, out)))
 
+    # The timed steps carry one event before and one after the whole step: an
+    # event between two kernels would stand between them in the stream and
+    # stop the next one from starting during the previous one's tail (the
+    # programmatic dependent launch the kernels are built for).  Per-kernel
+    # times come from a second loop with an event after every kernel.
     def step(ev):
+        ev[0].record(stream)
+        for _, run in stages:
+            run()
+        ev[1].record(stream)
+
+    def step_per_kernel(ev):
         ev[0].record(stream)
         for i, (_, run) in enumerate(stages):
             run()
             ev[i + 1].record(stream)
 
-    new_events = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)]
+    new_events = lambda n: [torch.cuda.Event(enable_timing=True) for _ in range(n)]
     for _ in range(args.warmup):
         flush_l2()
-        step(new_events())
+        step(new_events(2))
     torch.cuda.synchronize(dev)
     assert lay.error() == 0, "device error during warm-up"
 
-    evs = [new_events() for _ in range(args.steps)]
+    evs = [new_events(2) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize(dev)
     launches0 = binding.kernel_launches()
@@ -375,9 +386,16 @@ def run_native(args, rank, world, local):
     err = lay.error()
     assert err == 0, f"device error {err} in the timed region"
 
-    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(len(stages))] for e in evs])   # ms
-    step_ms = per.sum(axis=1)
+    step_ms = np.array([e[0].elapsed_time(e[1]) for e in evs])   # ms
     ms_per_step = reduce_max(float(step_ms.mean()), world, dev)
+    # Per-kernel breakdown (untimed for the headline): the same steps with an event after each kernel.
+    n_break = min(args.steps, args.breakdown_steps)
+    kevs = [new_events(len(stages) + 1) for _ in range(n_break)]
+    for i in range(n_break):
+        flush_l2()
+        step_per_kernel(kevs[i])
+    torch.cuda.synchronize(dev)
+    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(len(stages))] for e in kevs])   # ms
     kern_ms = dict(zip([name for name, _ in stages], per.mean(axis=0).tolist()))
     ab = algorithmic_bytes(w, lay, sf_cm)
     if ne:
@@ -466,6 +484,10 @@ def run_native(args, rank, world, local):
             "permute": ab["permute"] / permute_s / 1e9,
             "sf_col_major": (ab["sf_col_major"] / (kern_ms["sf_col_major"] / 1e3) / 1e9) if sf_cm else None,
             "combine": (ab["combine"] / (kern_ms["combine"] / 1e3) / 1e9) if do_combine else None},
+        "breakdown": {"steps": n_break, "sum_of_kernels_ms": float(sum(kern_ms.values())),
+                      "note": "kernels_ms come from separate steps with an event after every kernel; those "
+                              "events keep each kernel from starting during the previous one's tail, so their "
+                              "sum exceeds ms_per_step, which is timed per whole step"},
         "dispatch_tokens_per_s": world * N / (dispatch_ms / 1e3),
         "layout": {"valid_pairs": ab["P"], "rows": ab["rows"], "tokens_routed": ab["tokens_routed"]},
         "e2e": e2e_line,
@@ -546,6 +568,8 @@ def parse_args(argv=None):
     ap.add_argument("--sf-col-major", action="store_true",
                     help="fp8 workloads: scale factors column-major (TMA-aligned) by their own kernel")
     ap.add_argument("--ids-int32", action="store_true", help="--layout-only: int32 routing ids")
+    ap.add_argument("--breakdown-steps", type=int, default=300,
+                    help="steps of the per-kernel breakdown loop (after the timed steps)")
     ap.add_argument("--non-expand", action="store_true",
                     help="time the non-expand layout instead: layout, rank rows, rank-contiguous permute")
     ap.add_argument("--layout-only", action="store_true",

@@ -183,8 +183,18 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
   grid = max64(1, min64(grid, a.num_tokens));
   const int64_t max_tokens = max64(1, ceil_div64(a.num_tokens, grid));
   const size_t smem = (sizeof(int32_t) + sizeof(float)) * static_cast<size_t>(max_tokens) * a.topk;
-  const cudaError_t st = launch_pdl(combine_kernel, dim3(static_cast<unsigned>(grid)), dim3(kCombineThreads), smem,
-                                    stream, a, static_cast<int>(max_tokens));
+  // Small batches start during the previous kernel's tail (programmatic
+  // dependent launch); large ones start after it: measured on GB300, the
+  // overlap saved 1.2 us of a decode step and cost 26 us of a 131072-token one.
+  cudaError_t st;
+  if (small) {
+    st = launch_pdl(combine_kernel, dim3(static_cast<unsigned>(grid)), dim3(kCombineThreads), smem, stream, a,
+                    static_cast<int>(max_tokens));
+  } else {
+    combine_kernel<<<dim3(static_cast<unsigned>(grid)), dim3(kCombineThreads), smem, stream>>>(
+        a, static_cast<int>(max_tokens));
+    st = cudaGetLastError();
+  }
   if (st != cudaSuccess) return st;
   count_launch();
   return cudaSuccess;
