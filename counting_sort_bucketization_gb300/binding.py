@@ -95,6 +95,8 @@ def load_library() -> ctypes.CDLL:
         lib.moe_kernel_launches.restype = ctypes.c_uint64
         lib.moe_last_cuda_error.argtypes = [ctypes.POINTER(ctypes.c_char_p)]
         lib.moe_last_cuda_error.restype = ctypes.c_int
+        lib.moe_debug_set_waits.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32]
+        lib.moe_debug_set_waits.restype = ctypes.c_int
         for name in ("moe_layout_workspace_bytes", "moe_layout_count", "moe_layout_scan", "moe_layout_build",
                      "moe_layout_build_i32",
                      "moe_layout_rank_rows", "moe_dispatch_permute_ranks", "moe_dispatch_from_host",
@@ -108,6 +110,12 @@ def load_library() -> ctypes.CDLL:
 
 def strerror(status: int) -> str:
     return load_library().moe_strerror(int(status)).decode()
+
+
+def debug_set_waits(limit_ns: int = 0, barrier_extra: int = 0, extra_tx: int = 0) -> None:
+    """Test hook for the bounded waits (see moe_debug_set_waits); (0, 0, 0) restores normal operation."""
+    _check(load_library().moe_debug_set_waits(int(limit_ns), int(barrier_extra), int(extra_tx)),
+           "moe_debug_set_waits")
 
 
 def kernel_launches() -> int:

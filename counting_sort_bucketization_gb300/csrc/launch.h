@@ -62,6 +62,8 @@ struct PermuteArgs {
   int* err;
   unsigned* work;                // [2] token counter + finished-CTA counter (zero between launches)
   bool non_expand;               // rows of the non-expand layout (sizes the dynamic kernel's pieces)
+  uint64_t wait_ns;              // bound on each mbarrier wait (set by launch_permute)
+  unsigned extra_tx;             // test hook: bytes no copy delivers, on each CTA's first stage
 };
 
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t stream);
@@ -94,6 +96,15 @@ struct SfColMajorArgs {
 };
 
 cudaError_t launch_sf_col_major(const SfColMajorArgs& a, cudaStream_t stream);
+
+// Limit of every in-kernel wait and the test hooks that make a wait run out
+// (moe_debug_set_waits); the launchers copy them into the kernels' arguments.
+struct WaitConfig {
+  uint64_t limit_ns;        // bound on any in-kernel wait (default kWaitLimitNs)
+  unsigned barrier_extra;   // added to the fused layout's grid-barrier targets (0 in normal use)
+  unsigned extra_tx;        // bytes added to each CTA's first permute stage (0 in normal use)
+};
+WaitConfig wait_config();
 
 // Streaming multiprocessors of the current device (cached per device).
 int device_sm_count();

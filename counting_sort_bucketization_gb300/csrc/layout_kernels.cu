@@ -182,6 +182,8 @@ struct RankArgs {
   int64_t capacity;
   int32_t* total_rows;
   int* err;
+  uint64_t wait_ns;         // bound on each grid-barrier wait
+  unsigned barrier_extra;   // added to the grid-barrier targets: 0 except under the timeout test hook
 };
 
 // Rank of each pair among the same expert's pairs earlier in its warp's run
@@ -383,7 +385,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
 // arrivals resets the counter for the next launch on the workspace.  The
 // wait is bounded; on timeout the error word gets MOE_ERR_TIMEOUT and the CTA
 // stops (the counter then stays set: the workspace must be zeroed again).
-__device__ bool grid_barrier(unsigned* count, unsigned target, int* err, int* flag_s) {
+__device__ bool grid_barrier(unsigned* count, unsigned target, int* err, int* flag_s, uint64_t wait_ns) {
   __syncthreads();
   if (threadIdx.x == 0) {
     bool ok = true;
@@ -391,7 +393,7 @@ __device__ bool grid_barrier(unsigned* count, unsigned target, int* err, int* fl
     atomicAdd(count, 1u);
     const uint64_t t0 = ptx::globaltimer_ns();
     while (ptx::ld_acquire_gpu(count) < target) {
-      if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (ptx::globaltimer_ns() - t0 > wait_ns) {
         set_error(err, MOE_ERR_TIMEOUT);
         ok = false;
         break;
@@ -441,9 +443,9 @@ __global__ void __launch_bounds__(kLayoutThreads)
     hist[static_cast<int64_t>(e) * T + tile] = c;
   }
   for (int r = threadIdx.x; r < R; r += blockDim.x) rhist[static_cast<int64_t>(r) * T + tile] = rhist_s[r];
-  if (!grid_barrier(bar, gridDim.x, a.err, &flag_s)) return;
+  if (!grid_barrier(bar, gridDim.x + a.barrier_extra, a.err, &flag_s, a.wait_ns)) return;
   scan_phase(hist, rhist, plan.tiles, E, R, expert_count, rank_count);
-  if (!grid_barrier(bar, 2 * gridDim.x, a.err, &flag_s)) return;
+  if (!grid_barrier(bar, 2 * gridDim.x + a.barrier_extra, a.err, &flag_s, a.wait_ns)) return;
   grid_exit(bar, 2);
   rank_finish(plan, a, tile, tc, ids_s, off_s, cnt_s, lr_s, warp_tot_s);
 }
@@ -620,6 +622,9 @@ RankArgs rank_args(const moe_layout_desc& d, const int32_t* hist_prefix, const i
   a.capacity = capacity;
   a.total_rows = total_rows;
   a.err = err;
+  const WaitConfig wc = wait_config();
+  a.wait_ns = wc.limit_ns;
+  a.barrier_extra = wc.barrier_extra;
   return a;
 }
 

@@ -32,6 +32,15 @@ int device_sm_count() {
   return cache[dev];
 }
 
+static std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
+static std::atomic<unsigned> g_barrier_extra{0};
+static std::atomic<unsigned> g_extra_tx{0};
+
+WaitConfig wait_config() {
+  return WaitConfig{g_wait_limit_ns.load(std::memory_order_relaxed), g_barrier_extra.load(std::memory_order_relaxed),
+                    g_extra_tx.load(std::memory_order_relaxed)};
+}
+
 namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -328,6 +337,14 @@ const char* moe_strerror(int status) {
 }
 
 uint64_t moe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int moe_debug_set_waits(uint64_t limit_ns, uint32_t barrier_extra, uint32_t extra_tx) {
+  if (limit_ns > kWaitLimitNs || extra_tx % 16 != 0) return MOE_ERR_INVALID_ARG;
+  g_wait_limit_ns.store(limit_ns == 0 ? kWaitLimitNs : limit_ns, std::memory_order_relaxed);
+  g_barrier_extra.store(barrier_extra, std::memory_order_relaxed);
+  g_extra_tx.store(extra_tx, std::memory_order_relaxed);
+  return MOE_OK;
+}
 
 int moe_last_cuda_error(const char** message) {
   if (message != nullptr) *message = cudaGetErrorString(static_cast<cudaError_t>(t_last_cuda_error));

@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(kPermuteThreads)
     const uint64_t policy = store_policy();
     for (; u < units; ++u) {
       const int s = u % S;
-      if (!ptx::mbar_wait_parity_bounded(&full_bar[s], (u / S) & 1, kWaitLimitNs)) {
+      if (!ptx::mbar_wait_parity_bounded(&full_bar[s], (u / S) & 1, a.wait_ns)) {
         ok = false;
         break;
       }
@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(kPermuteThreads)
       set_error(a.err, MOE_ERR_TIMEOUT);
       // Let the loads already issued land before the CTA's shared memory goes away.
       for (int v = u; v < issued; ++v)
-        ptx::mbar_wait_parity_bounded(&full_bar[v % S], (v / S) & 1, kWaitLimitNs);
+        ptx::mbar_wait_parity_bounded(&full_bar[v % S], (v / S) & 1, a.wait_ns);
     }
     ptx::bulk_wait<0>();
     return;
@@ -475,7 +475,9 @@ __global__ void __launch_bounds__(kPermuteThreads, MOE_PERMUTE_DYN_MIN_BLOCKS)
     piece_of(u, t, off, len, with_sf);
     uint8_t* st = smem + static_cast<size_t>(npre) * p.stage_bytes;
     stage_tok[npre] = u;
-    ptx::mbar_expect_tx(&full_bar[npre], len + (with_sf ? static_cast<uint32_t>(p.sf_bytes) : 0u));
+    // a.extra_tx is 0 except under the timeout test hook: bytes no copy delivers.
+    ptx::mbar_expect_tx(&full_bar[npre], len + (with_sf ? static_cast<uint32_t>(p.sf_bytes) : 0u) +
+                                             (npre == 0 ? a.extra_tx : 0u));
     ptx::bulk_g2s(st, a.x + t * rb + off, len, &full_bar[npre]);
     if (with_sf)
       ptx::bulk_g2s(st + p.unit_bytes + p.slot_win, a.sf + t * srb, static_cast<uint32_t>(p.sf_bytes),
@@ -487,7 +489,7 @@ __global__ void __launch_bounds__(kPermuteThreads, MOE_PERMUTE_DYN_MIN_BLOCKS)
   if (!cap_ok) {
     if (blockIdx.x == 0) set_error(a.err, MOE_ERR_CAPACITY);
     for (int i = 0; i < npre; ++i) ptx::mbar_arrive(&full_bar[i]);
-    for (int i = 0; i < npre; ++i) ptx::mbar_wait_parity_bounded(&full_bar[i], 0, kWaitLimitNs);
+    for (int i = 0; i < npre; ++i) ptx::mbar_wait_parity_bounded(&full_bar[i], 0, a.wait_ns);
     return;   // no CTA touches the token counter
   }
   for (int i = 0; i < npre; ++i) {
@@ -540,7 +542,7 @@ __global__ void __launch_bounds__(kPermuteThreads, MOE_PERMUTE_DYN_MIN_BLOCKS)
   const uint64_t policy = store_policy();
   for (; j < issued; ++j) {
     const int s = static_cast<int>(j % S);
-    if (!ptx::mbar_wait_parity_bounded(&full_bar[s], static_cast<uint32_t>((j / S) & 1), kWaitLimitNs)) {
+    if (!ptx::mbar_wait_parity_bounded(&full_bar[s], static_cast<uint32_t>((j / S) & 1), a.wait_ns)) {
       ok = false;
       break;
     }
@@ -572,7 +574,7 @@ __global__ void __launch_bounds__(kPermuteThreads, MOE_PERMUTE_DYN_MIN_BLOCKS)
   if (!ok) {
     set_error(a.err, MOE_ERR_TIMEOUT);
     for (int64_t v = j; v < issued; ++v)
-      ptx::mbar_wait_parity_bounded(&full_bar[v % S], static_cast<uint32_t>((v / S) & 1), kWaitLimitNs);
+      ptx::mbar_wait_parity_bounded(&full_bar[v % S], static_cast<uint32_t>((v / S) & 1), a.wait_ns);
   }
   ptx::bulk_wait<0>();
   // The fence orders this CTA's claims before its arrival below; the last
@@ -650,7 +652,11 @@ int dyn_ctas_per_sm(size_t smem) {
 
 }  // namespace
 
-cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t stream) {
+cudaError_t launch_permute(const PermuteArgs& args, cudaStream_t stream) {
+  PermuteArgs a = args;
+  const WaitConfig wc = wait_config();
+  a.wait_ns = wc.limit_ns;
+  a.extra_tx = wc.extra_tx;
   if (dyn_applicable(a)) {
     DynPlan p = make_dyn_plan(a, 1);
     auto ctas_per_sm = [](size_t smem) {

@@ -348,6 +348,20 @@ MOE_API const char* moe_strerror(int status);
 MOE_API uint64_t moe_kernel_launches(void);
 
 /*
+ * Test hook for the bounded waits (not for normal use; process-wide; affects
+ * launches made after the call).  Every wait inside the library's kernels
+ * gives up after limit_ns nanoseconds (0: the default, 1 s; at most 1 s),
+ * records MOE_ERR_TIMEOUT and lets the kernel finish.  barrier_extra > 0
+ * raises the cooperative layout kernel's grid-barrier targets past the number
+ * of CTAs, so its first barrier can only run out; extra_tx (a multiple of 16)
+ * adds transaction bytes that no copy delivers to each CTA's first stage of
+ * the dynamic permute, so that stage can only run out.  A layout that timed
+ * out leaves its workspace's barrier counter set: zero the workspace before
+ * reusing it.  Call with (0, 0, 0) to restore normal operation.
+ */
+MOE_API int moe_debug_set_waits(uint64_t limit_ns, uint32_t barrier_extra, uint32_t extra_tx);
+
+/*
  * The CUDA error code (cudaError_t) behind this thread's most recent
  * MOE_ERR_CUDA, or 0 if there was none; *message (if non-NULL) receives its
  * description.  Diagnostics only: a status the pages do not define.

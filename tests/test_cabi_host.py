@@ -107,6 +107,15 @@ def test_last_cuda_error_is_readable_without_a_gpu(lib):
     assert lib.moe_last_cuda_error(None) == 0
 
 
+def test_wait_test_hook_checks_its_arguments(lib):
+    lib.moe_debug_set_waits.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32]
+    lib.moe_debug_set_waits.restype = ctypes.c_int
+    assert lib.moe_debug_set_waits(2_000_000_000, 0, 0) == 1   # longer than the 1 s bound
+    assert lib.moe_debug_set_waits(1_000_000, 0, 8) == 1       # bytes not a multiple of 16
+    assert lib.moe_debug_set_waits(1_000_000, 1, 16) == 0
+    assert lib.moe_debug_set_waits(0, 0, 0) == 0                # back to normal operation
+
+
 def test_strerror_and_launch_counter(lib):
     for code, name in binding.ERROR_NAMES.items():
         assert lib.moe_strerror(code)
