@@ -41,8 +41,8 @@ L2_FLUSH_BYTES = 256 << 20          # > 2x the 129 MB L2
 # DRAM traffic of the permute kernel from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), per launch, scaled to the decode workload, tied to
 # the kernel sources it was measured on.  bench reports null if they changed.
-PERMUTE_TRAFFIC = {"sha256": "aec3d083b3d155727c4d5b98ff24141c40276ae1a6d61a68a82d7f2465491159",
-                   "workload": "decode", "bytes_per_launch": 58_907_648 + 646_813_440}
+PERMUTE_TRAFFIC = {"sha256": "af146b045179bb8f8b2eee22ff3550533736ac2bf39a297aa3f7a69ae953988e",
+                   "workload": "decode", "bytes_per_launch": 58_951_680 + 647_970_816}
 PERMUTE_SOURCES = ["counting_sort_bucketization_gb300/csrc/permute_kernel.cu",
                    "counting_sort_bucketization_gb300/csrc/ptx.cuh",
                    "counting_sort_bucketization_gb300/csrc/common.cuh"]
