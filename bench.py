@@ -247,6 +247,8 @@ def run_layout_only(args, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = wl.WORKLOADS[args.workload]
+    if args.tokens is not None:
+        w = w.replace(num_tokens=args.tokens)
     idx = wl.draw_topk_idx(w, wl.SEEDS[w.name]).to(dev)
     if args.ids_int32:
         idx = idx.to(torch.int32)
@@ -568,6 +570,8 @@ def parse_args(argv=None):
     ap.add_argument("--sf-col-major", action="store_true",
                     help="fp8 workloads: scale factors column-major (TMA-aligned) by their own kernel")
     ap.add_argument("--ids-int32", action="store_true", help="--layout-only: int32 routing ids")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="--layout-only: tokens per batch instead of the workload's (same routing recipe)")
     ap.add_argument("--breakdown-steps", type=int, default=300,
                     help="steps of the per-kernel breakdown loop (after the timed steps)")
     ap.add_argument("--non-expand", action="store_true",

@@ -77,8 +77,14 @@ inline WorkspaceLayout make_workspace_layout(const moe_layout_desc& d, const Til
 // Launch with programmatic dependent launch allowed: the kernel may start
 // while the previous kernel on the stream is still running; it must execute
 // griddepcontrol.wait (ptx::grid_dependency_wait) before it reads anything
-// an earlier kernel wrote.  With any other predecessor (a copy, a kernel that
+// that kernel may write.  With any other predecessor (a copy, a kernel that
 // never triggers) it behaves like an ordinary launch.
+//
+// Every kernel of this library triggers its dependents only after its own
+// griddepcontrol.wait has returned.  So when a kernel of the library starts,
+// everything before its immediate predecessor on the stream has completed,
+// and it may read before its wait whatever no kernel of the library writes:
+// the routing ids (topk_idx) and the token rows and scale rows (x, sf).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                        Args&&... args) {

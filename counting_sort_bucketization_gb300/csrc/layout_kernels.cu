@@ -224,10 +224,10 @@ __device__ void rank_pass(const TilePlan& plan, int K, int E, int R, int ntok, c
 }
 
 // ids_s holds the tile's staged ids; cnt_s [kLayoutWarps*E] and lr_s come
-// from rank_pass; off_s [E+1] is shared scratch.  Offsets, the tile-0
-// outputs, absolute slots, the maps and the gap rows of src_idx.
+// from rank_pass; off_s [E+1] and gap_s [E] are shared scratch.  Offsets,
+// the tile-0 outputs, absolute slots, the maps and the gap rows of src_idx.
 __device__ void rank_finish(const TilePlan& plan, const RankArgs& a, int tile, TileCoords tc, const int* ids_s,
-                           int* off_s, int* cnt_s, int* lr_s, int* warp_tot_s) {
+                           int* off_s, int* gap_s, int* cnt_s, int* lr_s, int* warp_tot_s) {
   const int K = a.K, E = a.E, R = a.R, A = a.A;
   const int64_t T = plan.tiles;
   const int npairs = tc.ntok * K;
@@ -240,19 +240,23 @@ __device__ void rank_finish(const TilePlan& plan, const RankArgs& a, int tile, T
   constexpr int kPerThread = MOE_MAX_EXPERTS / kLayoutThreads;
   const int ipt = static_cast<int>(ceil_div64(E, kLayoutThreads));
   const int e_lo = threadIdx.x * ipt;
-  int aligned[kPerThread], prior[kPerThread];
+  int raw[kPerThread], prior[kPerThread];
 #pragma unroll
   for (int j = 0; j < kPerThread; ++j) {
     const int e = e_lo + j;
-    aligned[j] = (j < ipt && e < E) ? static_cast<int>(ceil_div64(__ldcg(a.expert_count + e), A) * A) : 0;
+    raw[j] = (j < ipt && e < E) ? __ldcg(a.expert_count + e) : 0;
     const int e2 = threadIdx.x + j * kLayoutThreads;
     prior[j] = (e2 < E && tile < T) ? __ldcg(a.hist_prefix + static_cast<int64_t>(e2) * T + tile) : 0;
   }
 
   // Aligned exclusive sum over experts ([CS] §7.2 then §5.5), block-wide.
+  int aligned[kPerThread];
   int mine = 0;
 #pragma unroll
-  for (int j = 0; j < kPerThread; ++j) mine += aligned[j];
+  for (int j = 0; j < kPerThread; ++j) {
+    aligned[j] = static_cast<int>(ceil_div64(raw[j], A) * A);
+    mine += aligned[j];
+  }
   const int incl = warp_inclusive_scan(mine, lane);
   if (lane == kWarpSize - 1) warp_tot_s[warp] = incl;
   __syncthreads();
@@ -264,6 +268,7 @@ __device__ void rank_finish(const TilePlan& plan, const RankArgs& a, int tile, T
     const int e = e_lo + j;
     if (j < ipt && e < E) {
       off_s[e] = run;
+      gap_s[e] = run + raw[j];   // first alignment-gap row of e
       run += aligned[j];
     }
   }
@@ -317,19 +322,14 @@ __device__ void rank_finish(const TilePlan& plan, const RankArgs& a, int tile, T
     a.dst_slot[tc.t0 * K + i] = slot;
   }
 
-  // Alignment-gap rows have no source token.
+  // Alignment-gap rows have no source token: one warp per expert, the gap's
+  // bounds already in shared memory (no global read per expert).
   if (cap_ok) {
-    for (int e = tile; e < E; e += gridDim.x) {
-      const int lo = off_s[e] + __ldcg(a.expert_count + e), hi = off_s[e + 1];
-      for (int row = lo + threadIdx.x; row < hi; row += blockDim.x) a.src_idx[row] = -1;
+    for (int e = tile * kLayoutWarps + warp; e < E; e += gridDim.x * kLayoutWarps) {
+      const int hi = off_s[e + 1];
+      for (int row = gap_s[e] + lane; row < hi; row += kWarpSize) a.src_idx[row] = -1;
     }
   }
-}
-
-__device__ void rank_phase(const TilePlan& plan, const RankArgs& a, int tile, TileCoords tc, const int* ids_s,
-                           int* off_s, int* cnt_s, int* lr_s, int* warp_tot_s) {
-  rank_pass(plan, a.K, a.E, a.R, tc.ntok, ids_s, cnt_s, lr_s, nullptr);
-  rank_finish(plan, a, tile, tc, ids_s, off_s, cnt_s, lr_s, warp_tot_s);
 }
 
 // ---------------------------------------------------------- kernels
@@ -360,22 +360,28 @@ __global__ void __launch_bounds__(kLayoutThreads)
   scan_phase(hist, rhist, T, E, R, expert_count, rank_count);
 }
 
+// The rank kernels stage their tile's ids and rank them inside each warp
+// before griddepcontrol.wait: the ids come from no kernel of this library, so
+// that part runs while the kernel before them (the column scan, or the layout)
+// is still working, and only the reads of the counts wait for it.
 template <typename IdT>
 __global__ void __launch_bounds__(kLayoutThreads)
     rank_maps_kernel(const IdT* __restrict__ topk_idx, TilePlan plan, RankArgs a) {
   extern __shared__ int smem[];
   int* off_s = smem;                            // [E+1]
-  int* cnt_s = off_s + (a.E + 1);               // [kLayoutWarps][E]
+  int* gap_s = off_s + (a.E + 1);               // [E]
+  int* cnt_s = gap_s + a.E;                     // [kLayoutWarps][E]
   int* ids_s = cnt_s + kLayoutWarps * a.E;      // [tile pairs]
   int* lr_s = ids_s + plan.tile_tokens * a.K;   // [tile pairs]
   __shared__ int warp_tot_s[kLayoutWarps];
   const TileCoords tc = tile_coords(plan, a.N, blockIdx.x);
   for (int i = threadIdx.x; i < kLayoutWarps * a.E; i += blockDim.x) cnt_s[i] = 0;
-  ptx::grid_dependency_wait();
-  ptx::grid_dependency_launch_dependents();
   stage_tile_ids(topk_idx, tc.t0 * a.K, tc.ntok * a.K, a.E, ids_s, a.err);
   __syncthreads();   // staged ids and zeroed counters visible to every warp
-  rank_phase(plan, a, blockIdx.x, tc, ids_s, off_s, cnt_s, lr_s, warp_tot_s);
+  rank_pass(plan, a.K, a.E, a.R, tc.ntok, ids_s, cnt_s, lr_s, nullptr);
+  ptx::grid_dependency_wait();
+  ptx::grid_dependency_launch_dependents();
+  rank_finish(plan, a, blockIdx.x, tc, ids_s, off_s, gap_s, cnt_s, lr_s, warp_tot_s);
 }
 
 // Grid-wide barrier for a cooperative launch on a counter that only grows
@@ -421,7 +427,8 @@ __global__ void __launch_bounds__(kLayoutThreads)
   int* lr_s = ids_s + plan.tile_tokens * K;     // [tile pairs]
   int* cnt_s = lr_s + plan.tile_tokens * K;     // [kLayoutWarps][E]
   int* off_s = cnt_s + kLayoutWarps * E;        // [E+1]
-  int* rhist_s = off_s + (E + 1);               // [R]
+  int* gap_s = off_s + (E + 1);                 // [E]
+  int* rhist_s = gap_s + E;                     // [R]
   __shared__ int warp_tot_s[kLayoutWarps];
   __shared__ int flag_s;
   const int tile = blockIdx.x;
@@ -447,7 +454,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
   scan_phase(hist, rhist, plan.tiles, E, R, expert_count, rank_count);
   if (!grid_barrier(bar, 2 * gridDim.x + a.barrier_extra, a.err, &flag_s, a.wait_ns)) return;
   grid_exit(bar, 2);
-  rank_finish(plan, a, tile, tc, ids_s, off_s, cnt_s, lr_s, warp_tot_s);
+  rank_finish(plan, a, tile, tc, ids_s, off_s, gap_s, cnt_s, lr_s, warp_tot_s);
 }
 
 // ------------------------------------------- non-expand rank rows
@@ -485,43 +492,10 @@ __global__ void __launch_bounds__(kLayoutThreads)
   const int64_t T = plan.tiles;
   const int warp = threadIdx.x / kWarpSize, lane = threadIdx.x % kWarpSize;
   for (int i = threadIdx.x; i < kLayoutWarps * R; i += blockDim.x) cnt_s[i] = 0;
-  ptx::grid_dependency_wait();
-  ptx::grid_dependency_launch_dependents();
+  // Before the wait (the ids come from no kernel of this library): stage the
+  // tile and rank each token's master lanes inside its warp.
   stage_tile_ids(topk_idx, tc.t0 * K, tc.ntok * K, E, ids_s, a.err);
-
-  // Block starts: exclusive sum of rank_count (thread i owns ranks [i*ipt, (i+1)*ipt)).
-  constexpr int kPerThread = MOE_MAX_EXPERTS / kLayoutThreads;
-  const int ipt = static_cast<int>(ceil_div64(R, kLayoutThreads));
-  const int r_lo = threadIdx.x * ipt;
-  int cnt[kPerThread], prior[kPerThread];
-#pragma unroll
-  for (int j = 0; j < kPerThread; ++j) {
-    const int r = r_lo + j;
-    cnt[j] = (j < ipt && r < R) ? __ldcg(a.rank_count + r) : 0;
-    const int r2 = threadIdx.x + j * kLayoutThreads;
-    prior[j] = (r2 < R && tile < T) ? __ldcg(a.rhist_prefix + static_cast<int64_t>(r2) * T + tile) : 0;
-  }
-  int mine = 0;
-#pragma unroll
-  for (int j = 0; j < kPerThread; ++j) mine += cnt[j];
-  const int incl = warp_inclusive_scan(mine, lane);
-  if (lane == kWarpSize - 1) warp_tot_s[warp] = incl;
   __syncthreads();
-  int run = incl - mine;
-  for (int w = 0; w < warp; ++w) run += warp_tot_s[w];
-#pragma unroll
-  for (int j = 0; j < kPerThread; ++j) {
-    const int r = r_lo + j;
-    if (j < ipt && r < R) {
-      start_s[r] = run;
-      run += cnt[j];
-    }
-  }
-  if (threadIdx.x == kLayoutThreads - 1) start_s[R] = run;
-  __syncthreads();
-  const bool cap_ok = start_s[R] <= a.capacity;
-  if (tile == 0 && threadIdx.x == 0 && !cap_ok) set_error(a.err, MOE_ERR_CAPACITY);
-
   const int tok_in_chunk = lane / K;
   int* my_cnt = cnt_s + warp * R;
   for (int c = 0; c < plan.cpw; ++c) {
@@ -544,7 +518,41 @@ __global__ void __launch_bounds__(kLayoutThreads)
     if (in) lr_s[pair] = master ? base + __popc(peers & ptx::lanemask_lt()) : -1;
     __syncwarp();
   }
+  ptx::grid_dependency_wait();
+  ptx::grid_dependency_launch_dependents();
+
+  // Block starts: exclusive sum of rank_count (thread i owns ranks [i*ipt, (i+1)*ipt)).
+  constexpr int kPerThread = MOE_MAX_EXPERTS / kLayoutThreads;
+  const int ipt = static_cast<int>(ceil_div64(R, kLayoutThreads));
+  const int r_lo = threadIdx.x * ipt;
+  int cnt[kPerThread], prior[kPerThread];
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) {
+    const int r = r_lo + j;
+    cnt[j] = (j < ipt && r < R) ? __ldcg(a.rank_count + r) : 0;
+    const int r2 = threadIdx.x + j * kLayoutThreads;
+    prior[j] = (r2 < R && tile < T) ? __ldcg(a.rhist_prefix + static_cast<int64_t>(r2) * T + tile) : 0;
+  }
+  int mine = 0;
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) mine += cnt[j];
+  const int incl = warp_inclusive_scan(mine, lane);
+  if (lane == kWarpSize - 1) warp_tot_s[warp] = incl;
+  __syncthreads();   // also: every warp's ranks and counters are in shared memory
+  int run = incl - mine;
+  for (int w = 0; w < warp; ++w) run += warp_tot_s[w];
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) {
+    const int r = r_lo + j;
+    if (j < ipt && r < R) {
+      start_s[r] = run;
+      run += cnt[j];
+    }
+  }
+  if (threadIdx.x == kLayoutThreads - 1) start_s[R] = run;
   __syncthreads();
+  const bool cap_ok = start_s[R] <= a.capacity;
+  if (tile == 0 && threadIdx.x == 0 && !cap_ok) set_error(a.err, MOE_ERR_CAPACITY);
 #pragma unroll
   for (int j = 0; j < kPerThread; ++j) {
     const int r = threadIdx.x + j * kLayoutThreads;
@@ -584,7 +592,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
 size_t fused_smem_bytes(const moe_layout_desc& d, const TilePlan& p) {
   const size_t pairs = static_cast<size_t>(p.tile_tokens) * d.topk;
   const size_t E = d.num_experts;
-  return sizeof(int) * (2 * pairs + kLayoutWarps * E + E + 1 + d.num_ranks);
+  return sizeof(int) * (2 * pairs + kLayoutWarps * E + 2 * E + 1 + d.num_ranks);
 }
 
 // Whether every tile's CTA of the fused kernel can be resident at once.
@@ -636,7 +644,7 @@ size_t count_smem_bytes(const moe_layout_desc& d, const TilePlan& p) {
 }
 
 size_t rank_smem_bytes(const moe_layout_desc& d, const TilePlan& p) {
-  return sizeof(int) * (static_cast<size_t>(d.num_experts) + 1 +
+  return sizeof(int) * (2 * static_cast<size_t>(d.num_experts) + 1 +
                         static_cast<size_t>(kLayoutWarps) * d.num_experts +
                         2 * static_cast<size_t>(p.tile_tokens) * d.topk);
 }

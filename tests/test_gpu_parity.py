@@ -209,10 +209,41 @@ def test_more_tiles_than_fit_at_once():
     w = _w(200000, 32, 64, 4, 16, H=16)
     idx = wl.draw_topk_idx(w, 31)
     ref = oracle.layout(idx.numpy(), 64, 4, 16)
+    rref = oracle.rank_layout(idx.numpy(), 64, 4)
     for fused in (True, False):
         lay = run_gpu_layout(w, idx, wl.worst_case_rows(w), fused=fused)
         assert lay.error() == 0
         assert_layout_matches(lay, ref, w)
+        # the non-expand map reads the rank prefix this path's column scan wrote
+        lay.rank_rows(idx.to(DEV), capacity_rows=rref["total_rows"])
+        assert lay.error() == 0
+        np.testing.assert_array_equal(lay.rank_slot.cpu().numpy().reshape(200000, 32), rref["rank_slot"])
+        np.testing.assert_array_equal(lay.rank_src.cpu().numpy(), rref["rank_src"])
+
+
+@pytest.mark.parametrize("w", [
+    _w(5, 8, 256, 8, 128, H=16),              # one tile; ~255 experts hold only gap rows
+    _w(32, 8, 256, 8, 128, H=16),             # one full tile, 32768 receive rows for 256 pairs
+    _w(512, 8, 256, 8, 128, H=16),
+    _w(736, 8, 256, 8, 128, H=16),
+    _w(100, 6, 1024, 1024, 1, H=16),          # E = R = 1024: the largest shared-memory plan of a tile
+], ids=lambda w: f"N{w.num_tokens}_E{w.num_experts}_R{w.num_ranks}_A{w.alignment}")
+def test_small_batches(w):
+    """Small batches at decode routing: few tiles, so each rank CTA writes the gap
+    rows of many experts (one warp per expert); the non-expand map follows."""
+    idx = wl.draw_topk_idx(w, 41)
+    ref = oracle.layout(idx.numpy(), w.num_experts, w.num_ranks, w.alignment)
+    before = binding.kernel_launches()
+    lay = run_gpu_layout(w, idx, wl.worst_case_rows(w), fused=True)
+    assert binding.kernel_launches() - before == 3      # count, column scan, rank
+    assert lay.error() == 0
+    assert_layout_matches(lay, ref, w)
+    rref = oracle.rank_layout(idx.numpy(), w.num_experts, w.num_ranks)
+    lay.rank_rows(idx.to(DEV), capacity_rows=rref["total_rows"])
+    assert lay.error() == 0
+    N, K = w.num_tokens, w.topk
+    np.testing.assert_array_equal(lay.rank_slot[: N * K].cpu().numpy().reshape(N, K), rref["rank_slot"])
+    np.testing.assert_array_equal(lay.rank_src.cpu().numpy(), rref["rank_src"])
 
 
 def test_empty_and_all_masked():
