@@ -41,8 +41,8 @@ L2_FLUSH_BYTES = 256 << 20          # > 2x the 129 MB L2
 # DRAM traffic of the permute kernel from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), per launch, scaled to the decode workload, tied to
 # the kernel sources it was measured on.  bench reports null if they changed.
-PERMUTE_TRAFFIC = {"sha256": "af146b045179bb8f8b2eee22ff3550533736ac2bf39a297aa3f7a69ae953988e",
-                   "workload": "decode", "bytes_per_launch": 58_951_680 + 647_970_816}
+PERMUTE_TRAFFIC = {"sha256": "84d1af49c0472e56db817dec3fd9e137f27bff7bb16289179472e7b8226b4aae",
+                   "workload": "decode", "bytes_per_launch": 58_915_840 + 646_384_640}
 PERMUTE_SOURCES = ["counting_sort_bucketization_gb300/csrc/permute_kernel.cu",
                    "counting_sort_bucketization_gb300/csrc/ptx.cuh",
                    "counting_sort_bucketization_gb300/csrc/common.cuh"]
