@@ -34,6 +34,17 @@
  *    expert's segment is its rank in (token, k) order among that expert's
  *    pairs, independent of scheduling.  ([CS] §6.2/§6.4 hand out slots with
  *    atomics instead, so their order varies from run to run.)
+ *  - Kernels are launched with programmatic dependent launch, and some of
+ *    them start reading their inputs topk_idx, x and sf before the kernel in
+ *    front of them on the stream has finished: the dispatch permutes prefetch
+ *    token rows, the rank kernels stage ids.  This is safe after copies, after
+ *    this library's own kernels (none of which writes those inputs) and after
+ *    any kernel that does not release its dependents early.  The kernel
+ *    launched on the stream directly before one of these calls must not write
+ *    the call's topk_idx, x or sf and also release its dependents before it
+ *    ends (griddepcontrol.launch_dependents /
+ *    cudaTriggerProgrammaticLaunchCompletion): put an event record or any
+ *    ordinary kernel between them.
  *
  * Kernels are compiled for sm_103a only.
  */
