@@ -18,6 +18,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -49,6 +50,18 @@ PERMUTE_SOURCES = ["counting_sort_bucketization_gb300/csrc/permute_kernel.cu",
 
 
 # ---------------------------------------------------------------- helpers
+def host_info() -> dict:
+    """The host the CPU baseline ran on: its CPU count and RAM (for the record; the
+    baseline itself is single-threaded)."""
+    info = {"host_cpus": os.cpu_count(), "host_arch": platform.machine()}
+    try:
+        pages, size = os.sysconf("SC_PHYS_PAGES"), os.sysconf("SC_PAGE_SIZE")
+        info["host_ram_gb"] = round(pages * size / 1e9, 1)
+    except (ValueError, OSError, AttributeError):
+        info["host_ram_gb"] = None
+    return info
+
+
 def sources_sha256(paths) -> str:
     h = hashlib.sha256()
     for p in paths:
@@ -508,7 +521,8 @@ def run_native(args, rank, world, local):
         tps, passes = runner.time_passes(args.cpu_seconds, args.cpu_max_passes)
         line["cpu_baseline"] = {"value": tps, "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": f"{passes} full pass(es) of the {w.name} workload ({N} tokens): "
-                                          f"layout, permute with zero padding, combine; single-threaded C"}
+                                          f"layout, permute with zero padding, combine; single-threaded C",
+                                **host_info()}
     print(json.dumps(line), flush=True)
 
 
@@ -546,7 +560,8 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / max(1, args.steps) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": config_of(w),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
+                         **host_info()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
