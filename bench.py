@@ -574,7 +574,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", choices=list(wl.WORKLOADS), default="decode")
-    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--e2e-steps", type=int, default=200,
+                    help="timed end-to-end steps (enough that filling and draining the batches in flight is ~1 %%)")
     ap.add_argument("--e2e-chunks", type=int, default=1, help="token chunks the host copies are split into")
     ap.add_argument("--e2e-lanes", type=int, default=3, help="batches in flight in the end-to-end leg")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

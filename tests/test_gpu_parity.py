@@ -367,6 +367,47 @@ def test_kernel_launch_counter_moves():
     assert binding.kernel_launches() - before == 3     # fused layout, permute, combine
 
 
+@pytest.mark.parametrize("w", [
+    _w(4096, 8, 256, 8, 128, H=64),      # the chained layout kernels
+    _w(20000, 8, 256, 8, 128, H=64),     # the cooperative layout kernel
+], ids=["chained", "cooperative"])
+def test_back_to_back_on_one_workspace(w):
+    """Three different routings through one workspace with no host synchronisation
+    between them: build, permute, combine, and device-side snapshots of the maps,
+    all queued on one stream.  Kernels that start before their predecessor ends
+    (reads before the PDL wait, the permute's counters reset by its last CTA) must
+    not mix one batch's state into the next."""
+    lay = binding.Layout(w, wl.worst_case_rows(w), device=DEV)
+    cap = wl.worst_case_rows(w)
+    batches = []
+    for seed in (61, 62, 63):
+        inp = wl.make(w, seed)
+        idx_d, x_d, wts_d = inp["topk_idx"].to(DEV), inp["x"].to(DEV), inp["weights"].to(DEV)
+        recv = torch.empty((cap, w.hidden), dtype=x_d.dtype, device=DEV)
+        out = torch.empty((w.num_tokens, w.hidden), dtype=torch.bfloat16, device=DEV)
+        lay.build(idx_d)
+        lay.permute(x_d, recv)
+        lay.combine(recv, wts_d, out)      # the identity stands in for the experts
+        snap = {k: getattr(lay, k).clone() for k in ("dst_slot", "src_idx", "expert_offset", "total_rows")}
+        batches.append((inp, recv, out, snap))
+    torch.cuda.synchronize()
+    assert lay.error() == 0
+    N, K = w.num_tokens, w.topk
+    for inp, recv, out, snap in batches:
+        ref = oracle.layout(inp["topk_idx"].numpy(), w.num_experts, w.num_ranks, w.alignment)
+        rows = ref["total_rows"]
+        assert int(snap["total_rows"].item()) == rows
+        np.testing.assert_array_equal(snap["expert_offset"].cpu().numpy(), ref["expert_offset"])
+        np.testing.assert_array_equal(snap["dst_slot"][: N * K].cpu().numpy().reshape(N, K), ref["dst_slot"])
+        np.testing.assert_array_equal(snap["src_idx"][:rows].cpu().numpy(), ref["src_idx"])
+        _, ref_recv, _ = oracle.permute(u8(inp["x"]), ref["dst_slot"], ref["expert_offset"], ref["expert_count"],
+                                        rows)
+        np.testing.assert_array_equal(u8(recv[:rows]), ref_recv)
+        ref_out = oracle.combine(ref_recv.view(np.uint16).reshape(rows, w.hidden), ref["dst_slot"],
+                                 inp["weights"].numpy())
+        check_combine(bf16_bits(out), ref_out)
+
+
 def test_cached_dispatch_reuses_the_layout():
     """Cached mode (the page keeps the slot map and skips counting on a second
     dispatch): the same dst_slot moves a second tensor with other row bytes."""
