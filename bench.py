@@ -39,11 +39,13 @@ UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20          # > 2x the 129 MB L2
 
-# DRAM traffic of the permute kernel from one ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum), per launch, scaled to the decode workload, tied to
-# the kernel sources it was measured on.  bench reports null if they changed.
+# DRAM traffic of the permute kernel from ncu captures (dram__bytes_read.sum +
+# dram__bytes_write.sum) per launch, by workload and layout mode, tied to the
+# kernel sources they were measured on.  bench reports null if they changed
+# or the workload was not captured.
 PERMUTE_TRAFFIC = {"sha256": "84d1af49c0472e56db817dec3fd9e137f27bff7bb16289179472e7b8226b4aae",
-                   "workload": "decode", "bytes_per_launch": 58_915_840 + 646_384_640}
+                   "bytes_per_launch": {"decode": 58_915_840 + 646_384_640,
+                                        "decode/non-expand": 58_925_568 + 249_672_704}}
 PERMUTE_SOURCES = ["counting_sort_bucketization_gb300/csrc/permute_kernel.cu",
                    "counting_sort_bucketization_gb300/csrc/ptx.cuh",
                    "counting_sort_bucketization_gb300/csrc/common.cuh"]
@@ -479,9 +481,8 @@ def run_native(args, rank, world, local):
     permute_s = kern_ms[dom] / 1e3
     achieved = ab[dom] / permute_s / 1e9
     traffic = None
-    if not ne and PERMUTE_TRAFFIC and PERMUTE_TRAFFIC.get("sha256") == sources_sha256(PERMUTE_SOURCES) \
-            and PERMUTE_TRAFFIC.get("workload") == w.name:
-        traffic = PERMUTE_TRAFFIC["bytes_per_launch"]
+    if PERMUTE_TRAFFIC.get("sha256") == sources_sha256(PERMUTE_SOURCES):
+        traffic = PERMUTE_TRAFFIC["bytes_per_launch"].get(w.name + ("/non-expand" if ne else ""))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
