@@ -45,7 +45,9 @@ L2_FLUSH_BYTES = 256 << 20          # > 2x the 129 MB L2
 # or the workload was not captured.
 PERMUTE_TRAFFIC = {"sha256": "84d1af49c0472e56db817dec3fd9e137f27bff7bb16289179472e7b8226b4aae",
                    "bytes_per_launch": {"decode": 58_915_840 + 646_384_640,
-                                        "decode/non-expand": 58_925_568 + 249_672_704}}
+                                        "decode/non-expand": 58_925_568 + 249_672_704,
+                                        "skewed": 235_471_616 + 1_841_223_936,
+                                        "prefill_fp8": 243_337_984 + 1_997_432_064}}
 PERMUTE_SOURCES = ["counting_sort_bucketization_gb300/csrc/permute_kernel.cu",
                    "counting_sort_bucketization_gb300/csrc/ptx.cuh",
                    "counting_sort_bucketization_gb300/csrc/common.cuh"]
