@@ -81,6 +81,20 @@ __device__ __forceinline__ int warp_inclusive_scan(int v, int lane) {
   return v;
 }
 
+// Exclusive prefix of `mine` over the block's threads in thread order, for
+// blocks whose threads each own a contiguous run of the items being summed:
+// a warp scan, then the warps' totals through shared memory.  Contains a
+// __syncthreads, so it also publishes the block's earlier shared writes.
+__device__ __forceinline__ int block_exclusive_base(int mine, int* warp_tot_s) {
+  const int warp = threadIdx.x / kWarpSize, lane = threadIdx.x % kWarpSize;
+  const int incl = warp_inclusive_scan(mine, lane);
+  if (lane == kWarpSize - 1) warp_tot_s[warp] = incl;
+  __syncthreads();
+  int base = incl - mine;
+  for (int w = 0; w < warp; ++w) base += warp_tot_s[w];
+  return base;
+}
+
 struct TileCoords {
   int64_t t0;   // first token of the tile
   int ntok;     // tokens in the tile (the last tile may be short)
@@ -257,12 +271,7 @@ __device__ void rank_finish(const TilePlan& plan, const RankArgs& a, int tile, T
     aligned[j] = static_cast<int>(ceil_div64(raw[j], A) * A);
     mine += aligned[j];
   }
-  const int incl = warp_inclusive_scan(mine, lane);
-  if (lane == kWarpSize - 1) warp_tot_s[warp] = incl;
-  __syncthreads();
-  int warp_base = 0;
-  for (int w = 0; w < warp; ++w) warp_base += warp_tot_s[w];
-  int run = warp_base + incl - mine;
+  int run = block_exclusive_base(mine, warp_tot_s);
 #pragma unroll
   for (int j = 0; j < kPerThread; ++j) {
     const int e = e_lo + j;
@@ -536,11 +545,8 @@ __global__ void __launch_bounds__(kLayoutThreads)
   int mine = 0;
 #pragma unroll
   for (int j = 0; j < kPerThread; ++j) mine += cnt[j];
-  const int incl = warp_inclusive_scan(mine, lane);
-  if (lane == kWarpSize - 1) warp_tot_s[warp] = incl;
-  __syncthreads();   // also: every warp's ranks and counters are in shared memory
-  int run = incl - mine;
-  for (int w = 0; w < warp; ++w) run += warp_tot_s[w];
+  // (its barrier also publishes every warp's ranks and counters)
+  int run = block_exclusive_base(mine, warp_tot_s);
 #pragma unroll
   for (int j = 0; j < kPerThread; ++j) {
     const int r = r_lo + j;
