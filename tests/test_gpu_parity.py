@@ -44,9 +44,14 @@ def bf16_bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
 
 
+SENTINEL_MAP = -9   # canary in src_idx: entries past the layout's rows must keep it
+
+
 def run_gpu_layout(w, idx_cpu, cap, fused=True):
-    lay = binding.Layout(w, cap, device=DEV).build(idx_cpu.to(DEV), fused=fused)
-    return lay
+    lay = binding.Layout(w, cap, device=DEV)
+    lay.src_idx.fill_(SENTINEL_MAP)
+    lay.src_canary = True
+    return lay.build(idx_cpu.to(DEV), fused=fused)
 
 
 def assert_layout_matches(lay, ref, w, check_src=True):
@@ -57,7 +62,10 @@ def assert_layout_matches(lay, ref, w, check_src=True):
     np.testing.assert_array_equal(lay.dst_slot[: N * K].cpu().numpy().reshape(N, K), ref["dst_slot"])
     if check_src:
         rows = ref["total_rows"]
-        np.testing.assert_array_equal(lay.src_idx[:rows].cpu().numpy(), ref["src_idx"])
+        src = lay.src_idx.cpu().numpy()
+        np.testing.assert_array_equal(src[:rows], ref["src_idx"])
+        if getattr(lay, "src_canary", False):
+            assert np.all(src[rows:] == SENTINEL_MAP), "src_idx written past the layout's rows"
 
 
 def scale_rows_on_gpu(recv, expert_offset, scale, rows):
@@ -101,17 +109,29 @@ def full_case(w: wl.Workload, seed: int, combine=True, cap=None, fused=True):
     np.testing.assert_array_equal(u8(recv[:rows]), ref_recv)
     if sf is not None:
         np.testing.assert_array_equal(u8(recv_sf[:rows]), ref_sf)
+    # Canaries: receive rows past the layout's keep their fill, and the inputs are not written.
+    fill = 0x5A if x.element_size() == 1 else None
+    tail = u8(recv[rows:])
+    assert np.all(tail == fill) if fill is not None else bool(torch.all(recv[rows:] == -7.0)), \
+        "receive rows written past the layout's rows"
+    if sf is not None:
+        assert bool(torch.all(recv_sf[rows:] == -3.0)), "scale rows written past the layout's rows"
+        np.testing.assert_array_equal(u8(sf), u8(inp["sf"]))
+    np.testing.assert_array_equal(u8(x), u8(inp["x"]))
     if combine and w.row_dtype == "bf16":
         scale = inp["expert_scale"]
         eo = scale_rows_on_gpu(recv, lay.expert_offset, scale, rows)
         ref_eo = oracle.expert_scale(ref_recv.view(np.uint16).reshape(rows, w.hidden), ref["expert_offset"],
                                      scale.numpy())
         np.testing.assert_array_equal(bf16_bits(eo), ref_eo)
-        out = torch.empty((w.num_tokens, w.hidden), dtype=torch.bfloat16, device=DEV)
+        # one guard row past the N output rows
+        out_guard = torch.full((w.num_tokens + 1, w.hidden), 5.0, dtype=torch.bfloat16, device=DEV)
+        out = out_guard[: w.num_tokens]
         lay.combine(eo, inp["weights"].to(DEV), out)
         assert lay.error() == 0
         ref_out = oracle.combine(ref_eo, ref["dst_slot"], inp["weights"].numpy())
         check_combine(bf16_bits(out), ref_out)
+        assert bool(torch.all(out_guard[w.num_tokens] == 5.0)), "combine wrote past its N rows"
     return lay, recv
 
 
