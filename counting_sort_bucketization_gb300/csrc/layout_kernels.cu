@@ -28,6 +28,8 @@
 //     their gaps disappear.  Its barrier waits are bounded (MOE_ERR_TIMEOUT).
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "launch.h"
 #include "ptx.cuh"
@@ -710,8 +712,10 @@ cudaError_t launch_rank_rows_t(const moe_layout_desc& d, const TilePlan& p, cons
   return cudaSuccess;
 }
 
-bool& fused_pdl_refused() {
-  static bool refused = false;
+// Set once a driver has refused the cooperative + PDL launch pair; read by
+// every later build, from any host thread.
+std::atomic<bool>& fused_pdl_refused() {
+  static std::atomic<bool> refused{false};
   return refused;
 }
 
@@ -743,12 +747,12 @@ cudaError_t launch_build_t(const moe_layout_desc& d, const TilePlan& p, const Id
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = fused_pdl_refused() ? 1 : 2;
+  cfg.numAttrs = fused_pdl_refused().load(std::memory_order_relaxed) ? 1 : 2;
   cudaError_t st = cudaLaunchKernelEx(&cfg, layout_fused_kernel<IdT>, topk_idx, p, a, hist, rhist, expert_count,
                                       rank_count, barrier_words);
   if (st != cudaSuccess && cfg.numAttrs == 2) {
     (void)cudaGetLastError();
-    fused_pdl_refused() = true;
+    fused_pdl_refused().store(true, std::memory_order_relaxed);
     cfg.numAttrs = 1;
     st = cudaLaunchKernelEx(&cfg, layout_fused_kernel<IdT>, topk_idx, p, a, hist, rhist, expert_count, rank_count,
                             barrier_words);
