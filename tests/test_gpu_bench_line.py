@@ -1,0 +1,45 @@
+"""bench.py's native JSON line on a GB300: one line, with every key the
+benchmark contract asks for and the types it asks for (a short run of the
+decode workload: 5 timed steps after 3 warm-up steps)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+REPO = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _number(v):
+    return isinstance(v, (int, float)) and not isinstance(v, bool)
+
+
+def test_native_line_keeps_the_contract():
+    proc = subprocess.run([sys.executable, os.path.join(REPO, "bench.py"), "--steps", "5", "--warmup", "3",
+                           "--e2e-steps", "5", "--breakdown-steps", "5", "--cpu-seconds", "1",
+                           "--cpu-max-passes", "1"],
+                          cwd=REPO, capture_output=True, text=True, timeout=600)
+    assert proc.returncode == 0, proc.stderr[-3000:]
+    lines = [ln for ln in proc.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1, proc.stdout
+    d = json.loads(lines[0])
+    import bench
+    assert d["metric"] == bench.METRIC and d["unit"] == "tokens/s"
+    assert _number(d["value"]) and d["value"] > 0 and _number(d["ms_per_step"]) and d["ms_per_step"] > 0
+    assert d["n_gpus"] == 1 and d["steps"] == 5 and d["warmup"] == 3
+    assert d["higher_is_better"] is True and d["scaling"] == "weak" and d["vs_baseline"] is None
+    assert d["dtype"] == "bf16" and d["data"] == "synthetic" and d["config"]["workload"] == "decode"
+    rf = d["roofline"]
+    assert rf["bound"] == "hbm" and rf["unit"] == "GB/s"
+    assert _number(rf["achieved"]) and _number(rf["peak"]) and abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-9
+    assert rf["traffic"] is None or _number(rf["traffic"])
+    e2e = d["e2e"]
+    assert _number(e2e["value"]) and e2e["value"] > 0 and e2e["unit"] == "tokens/s"
+    assert e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
+    assert isinstance(d["gpu_launches"], int) and d["gpu_launches"] >= 5 * 3
+    assert "clocks" in d
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["unit"] == "tokens/s" and _number(cb["value"])
