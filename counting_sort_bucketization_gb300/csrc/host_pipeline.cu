@@ -55,6 +55,8 @@ extern "C" int moe_dispatch_from_host(const moe_layout_desc* desc, const int64_t
   if ((weights_host == nullptr) != (weights == nullptr) || (sf_host == nullptr) != (sf == nullptr) ||
       row_bytes <= 0 || chunk_tokens < 0)
     return MOE_ERR_INVALID_ARG;
+  if (row_bytes > MOE_MAX_ROW_BYTES || (sf_host != nullptr && sf_row_bytes > MOE_MAX_ROW_BYTES))
+    return MOE_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaStream_t cs = static_cast<cudaStream_t>(copy_stream);
   CallEvent e;
@@ -109,6 +111,7 @@ extern "C" int moe_combine_to_host(const moe_layout_desc* desc, const void* expe
   const int K = desc->topk;
   if ((N > 0 && (out == nullptr || out_host == nullptr)) || hidden <= 0 || chunk_tokens < 0)
     return MOE_ERR_INVALID_ARG;
+  if (hidden > MOE_MAX_ROW_BYTES / 2) return MOE_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaStream_t cs = static_cast<cudaStream_t>(copy_stream);
   CallEvent e;

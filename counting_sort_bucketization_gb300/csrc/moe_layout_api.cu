@@ -51,10 +51,11 @@ int check_desc(const moe_layout_desc* d) {
     return MOE_ERR_INVALID_ARG;
   if (d->num_experts % d->num_ranks != 0) return MOE_ERR_INVALID_ARG;
   if (d->topk > MOE_MAX_TOPK || d->num_experts > MOE_MAX_EXPERTS) return MOE_ERR_UNSUPPORTED;
-  // Every slot and row index must fit int32.
+  // Every slot and row index must fit int32.  N is bounded first, so that
+  // N * K is only formed when it cannot overflow.
+  if (d->num_tokens > (int64_t{1} << 31) / d->topk) return MOE_ERR_UNSUPPORTED;
   const int64_t worst = d->num_tokens * d->topk + static_cast<int64_t>(d->num_experts) * (d->alignment - 1);
-  if (d->num_tokens > (int64_t{1} << 31) / d->topk || worst >= (int64_t{1} << 31))
-    return MOE_ERR_UNSUPPORTED;
+  if (worst >= (int64_t{1} << 31)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -176,6 +177,7 @@ int moe_dispatch_permute(const moe_layout_desc* desc, const void* x, int64_t row
         (capacity_rows > 0 && recv_sf == nullptr))
       return MOE_ERR_INVALID_ARG;
   }
+  if (row_bytes > MOE_MAX_ROW_BYTES || (sf != nullptr && sf_row_bytes > MOE_MAX_ROW_BYTES)) return MOE_ERR_UNSUPPORTED;
   PermuteArgs a{};
   a.x = static_cast<const uint8_t*>(x);
   a.sf = static_cast<const uint8_t*>(sf);
@@ -230,6 +232,7 @@ int moe_dispatch_permute_ranks(const moe_layout_desc* desc, const void* x, int64
         (capacity_rows > 0 && recv_sf == nullptr))
       return MOE_ERR_INVALID_ARG;
   }
+  if (row_bytes > MOE_MAX_ROW_BYTES || (sf != nullptr && sf_row_bytes > MOE_MAX_ROW_BYTES)) return MOE_ERR_UNSUPPORTED;
   PermuteArgs a{};
   a.x = static_cast<const uint8_t*>(x);
   a.sf = static_cast<const uint8_t*>(sf);
@@ -263,6 +266,7 @@ int moe_dispatch_sf_col_major(const moe_layout_desc* desc, const void* sf, int64
   if ((desc->num_tokens > 0 && sf == nullptr) || (capacity_rows > 0 && (src == nullptr || recv_sf_cm == nullptr)))
     return MOE_ERR_INVALID_ARG;
   if (!aligned(sf, 4) || !aligned(recv_sf_cm, 16)) return MOE_ERR_INVALID_ARG;
+  if (sf_cols > MOE_MAX_ROW_BYTES / 4 || ld > (int64_t{1} << 32)) return MOE_ERR_UNSUPPORTED;
   SfColMajorArgs a{};
   a.sf = static_cast<const uint32_t*>(sf);
   a.cols = sf_cols;
@@ -284,6 +288,7 @@ int moe_combine_unpermute(const moe_layout_desc* desc, const void* expert_out, i
   WorkspaceLayout w;
   if (int st = check_workspace(desc, workspace, workspace_bytes, &w)) return st;
   if (hidden <= 0 || hidden % 8 != 0 || expert_out_rows < 0) return MOE_ERR_INVALID_ARG;
+  if (hidden > MOE_MAX_ROW_BYTES / 2) return MOE_ERR_UNSUPPORTED;
   if (desc->num_tokens == 0) return MOE_OK;
   if (dst_slot == nullptr || weights == nullptr || out == nullptr ||
       (expert_out_rows > 0 && expert_out == nullptr))

@@ -76,9 +76,12 @@ enum moe_status {
   MOE_ERR_UNSUPPORTED = 6    /* host: sizes beyond what this build supports            */
 };
 
-/* Limits of this build. */
+/* Limits of this build.  Rows (token rows, scale rows, combine rows of
+ * 2 * hidden bytes) longer than MOE_MAX_ROW_BYTES are refused with
+ * MOE_ERR_UNSUPPORTED, which keeps every byte offset well inside int64. */
 #define MOE_MAX_TOPK 32
 #define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_ROW_BYTES (1 << 30)
 
 /* Problem description.  Plain values, copied by every call. */
 typedef struct moe_layout_desc {
@@ -234,6 +237,8 @@ MOE_API int moe_dispatch_permute_ranks(const moe_layout_desc* desc, const void* 
  *        moe_layout_build, or rank_psum + R - 1;
  *   recv_sf_cm [sf_cols, ld] words, 16-byte aligned, ld >= capacity_rows,
  *        ld a multiple of 4.
+ * sf_cols above MOE_MAX_ROW_BYTES / 4 or ld above 2^32 return
+ * MOE_ERR_UNSUPPORTED.
  * rows > capacity_rows records MOE_ERR_CAPACITY and nothing is written; a
  * src entry outside [-1, N) is skipped and records MOE_ERR_INVALID_ARG.
  * Independent of moe_dispatch_permute: call it instead of passing sf there,

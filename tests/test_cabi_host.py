@@ -98,6 +98,26 @@ def test_host_checks_reject_before_launch(lib):
     assert lib.moe_layout_get_error(None, None, None) == 1
 
 
+def test_oversized_rows_are_refused_before_launch(lib):
+    """Rows past MOE_MAX_ROW_BYTES (2^30) return MOE_ERR_UNSUPPORTED (6): every
+    byte offset stays well inside int64."""
+    d = ctypes.byref(_desc())
+    n = ctypes.c_size_t(0)
+    lib.moe_layout_workspace_bytes(d, ctypes.byref(n))
+    fake = ctypes.c_void_p(1 << 20)         # never dereferenced
+    big = (1 << 30) + 16
+    args = lambda rb, sf, srb: (d, fake, rb, sf, srb, fake, fake, fake, fake, fake if sf else None, 100, 1, fake,
+                                n.value, None)
+    assert lib.moe_dispatch_permute(*args(big, None, 0)) == 6
+    assert lib.moe_dispatch_permute(*args(32, fake, big)) == 6
+    ranks = lambda rb: (d, fake, rb, None, 0, fake, fake, fake, None, 100, fake, n.value, None)
+    assert lib.moe_dispatch_permute_ranks(*ranks(big)) == 6
+    assert lib.moe_combine_unpermute(d, fake, 10, (1 << 29) + 8, fake, fake, fake, fake, n.value, None) == 6
+    sfa = lambda C, ld: (d, fake, C, fake, fake, fake, ld, 100, 1, fake, n.value, None)
+    assert lib.moe_dispatch_sf_col_major(*sfa((1 << 28) + 1, 100)) == 6
+    assert lib.moe_dispatch_sf_col_major(*sfa(56, (1 << 32) + 4)) == 6
+
+
 def test_last_cuda_error_is_readable_without_a_gpu(lib):
     lib.moe_last_cuda_error.argtypes = [ctypes.POINTER(ctypes.c_char_p)]
     lib.moe_last_cuda_error.restype = ctypes.c_int
