@@ -137,7 +137,11 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _dev(t: torch.Tensor | None, name: str, dtype=None, numel=None, allow_none=False):
+def _nbytes(t: torch.Tensor) -> int:
+    return t.numel() * t.element_size()
+
+
+def _dev(t: torch.Tensor | None, name: str, dtype=None, numel=None, allow_none=False, nbytes=None):
     if t is None:
         if allow_none:
             return None
@@ -150,6 +154,8 @@ def _dev(t: torch.Tensor | None, name: str, dtype=None, numel=None, allow_none=F
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if numel is not None and t.numel() < numel:
         raise ValueError(f"{name} needs at least {numel} elements, has {t.numel()}")
+    if nbytes is not None and _nbytes(t) < nbytes:
+        raise ValueError(f"{name} needs at least {nbytes} bytes, has {_nbytes(t)}")
     return ctypes.c_void_p(t.data_ptr())
 
 
@@ -225,7 +231,8 @@ def dispatch_permute(desc, x, dst_slot, expert_offset, expert_count, recv_x, wor
         if recv_sf is None or recv_sf.shape[0] != cap or recv_sf.numel() * recv_sf.element_size() != cap * srb:
             raise ValueError("recv_sf must be [capacity, sf row] when sf is given")
     st = load_library().moe_dispatch_permute(
-        ctypes.byref(_desc(desc)), _dev(x, "x"), rb, _dev(sf, "sf", allow_none=True), srb,
+        ctypes.byref(_desc(desc)), _dev(x, "x", nbytes=N * rb), rb, _dev(sf, "sf", allow_none=True, nbytes=N * srb),
+        srb,
         _dev(dst_slot, "dst_slot", torch.int32, N * K), _dev(expert_offset, "expert_offset", torch.int32, E + 1),
         _dev(expert_count, "expert_count", torch.int32, E), _dev(recv_x, "recv_x"),
         _dev(recv_sf, "recv_sf", allow_none=True), cap, 1 if zero_pad else 0,
@@ -258,7 +265,8 @@ def dispatch_permute_ranks(desc, x, rank_slot, rank_psum, recv, workspace, sf=No
         if recv_sf is None or recv_sf.shape[0] != cap or recv_sf.numel() * recv_sf.element_size() != cap * srb:
             raise ValueError("recv_sf must be [capacity, sf row] when sf is given")
     st = load_library().moe_dispatch_permute_ranks(
-        ctypes.byref(_desc(desc)), _dev(x, "x"), rb, _dev(sf, "sf", allow_none=True), srb,
+        ctypes.byref(_desc(desc)), _dev(x, "x", nbytes=N * rb), rb, _dev(sf, "sf", allow_none=True, nbytes=N * srb),
+        srb,
         _dev(rank_slot, "rank_slot", torch.int32, N * K), _dev(rank_psum, "rank_psum", torch.int32, R),
         _dev(recv, "recv"), _dev(recv_sf, "recv_sf", allow_none=True), cap,
         _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
@@ -315,13 +323,15 @@ def accumulate_stats(desc, expert_count, cumulative, stream=None) -> None:
     _check(st, "moe_layout_accumulate_stats")
 
 
-def _host(t: torch.Tensor | None, name: str, allow_none=False):
+def _host(t: torch.Tensor | None, name: str, allow_none=False, nbytes=None):
     if t is None:
         if allow_none:
             return None
         raise ValueError(f"{name} is required")
     if t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous host tensor (page-locked for overlap)")
+    if nbytes is not None and _nbytes(t) < nbytes:
+        raise ValueError(f"{name} needs at least {nbytes} bytes, has {_nbytes(t)}")
     return ctypes.c_void_p(t.data_ptr())
 
 
@@ -343,14 +353,18 @@ def dispatch_from_host(lay: "Layout", topk_idx_host, x_host, topk_idx, x, recv_x
     rb = x_host.shape[1] * x_host.element_size()
     srb = sf_host.shape[1] * sf_host.element_size() if sf_host is not None else 0
     st = load_library().moe_dispatch_from_host(
-        ctypes.byref(_desc(d)), _host(topk_idx_host, "topk_idx_host"), _host(x_host, "x_host"), rb,
-        _host(sf_host, "sf_host", True), srb, _host(weights_host, "weights_host", True),
-        _dev(topk_idx, "topk_idx", torch.int64, N * K), _dev(x, "x"), _dev(sf, "sf", allow_none=True),
+        ctypes.byref(_desc(d)), _host(topk_idx_host, "topk_idx_host", nbytes=8 * N * K),
+        _host(x_host, "x_host", nbytes=N * rb), rb, _host(sf_host, "sf_host", True, nbytes=N * srb), srb,
+        _host(weights_host, "weights_host", True, nbytes=4 * N * K),
+        _dev(topk_idx, "topk_idx", torch.int64, N * K), _dev(x, "x", nbytes=N * rb),
+        _dev(sf, "sf", allow_none=True, nbytes=N * srb),
         _dev(weights, "weights", torch.float32, N * K, allow_none=True),
         _dev(lay.expert_count, "expert_count"), _dev(lay.rank_count, "rank_count"),
         _dev(lay.expert_offset, "expert_offset"), _dev(lay.rank_psum, "rank_psum"), _dev(lay.dst_slot, "dst_slot"),
-        _dev(lay.src_idx, "src_idx"), _dev(lay.total_rows, "total_rows"), _dev(recv_x, "recv_x"),
-        _dev(recv_sf, "recv_sf", allow_none=True), recv_x.shape[0], _dev(lay.workspace, "workspace"),
+        _dev(lay.src_idx, "src_idx"), _dev(lay.total_rows, "total_rows"),
+        _dev(recv_x, "recv_x", nbytes=recv_x.shape[0] * rb),
+        _dev(recv_sf, "recv_sf", allow_none=True, nbytes=recv_x.shape[0] * srb), recv_x.shape[0],
+        _dev(lay.workspace, "workspace"),
         lay.workspace.numel(), int(chunk_tokens), _stream_ptr(s), _stream_ptr(copy_stream))
     _check(st, "moe_dispatch_from_host")
 
@@ -370,7 +384,9 @@ def combine_to_host(lay: "Layout", expert_out, weights, out, out_host, chunk_tok
     st = load_library().moe_combine_to_host(
         ctypes.byref(_desc(d)), _dev(expert_out, "expert_out"), expert_out.shape[0], expert_out.shape[1],
         _dev(lay.dst_slot, "dst_slot", torch.int32, N * K), _dev(weights, "weights", torch.float32, N * K),
-        _dev(out, "out"), _host(out_host, "out_host"), _dev(lay.workspace, "workspace"), lay.workspace.numel(),
+        _dev(out, "out", nbytes=2 * N * expert_out.shape[1]),
+        _host(out_host, "out_host", nbytes=2 * N * expert_out.shape[1]), _dev(lay.workspace, "workspace"),
+        lay.workspace.numel(),
         int(chunk_tokens), _stream_ptr(s), _stream_ptr(copy_stream))
     _check(st, "moe_combine_to_host")
 

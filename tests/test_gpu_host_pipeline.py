@@ -147,3 +147,27 @@ def test_pipelined_dispatch_only_fp8():
         if i == len(batches) - 1:   # the lane of the last batch still holds its scale rows
             lane = pipe.lane(i % pipe.lanes)
             np.testing.assert_array_equal(u8(lane["recv_sf"][:rows]), want_sf)
+
+
+def test_short_buffers_are_refused_before_anything_runs():
+    # host or device buffers smaller than N rows: the binding raises, nothing is copied or launched
+    w = wl.WORKLOADS["tiny"]
+    cap = wl.worst_case_rows(w)
+    inp = wl.make(w, 31)
+    N, H = w.num_tokens, w.hidden
+    lay = binding.Layout(w, cap, device=DEV).build(inp["topk_idx"].to(DEV))
+    x = inp["x"].to(DEV)
+    recv = torch.empty((cap, H), dtype=x.dtype, device=DEV)
+    launches = binding.kernel_launches()
+    with pytest.raises(ValueError, match="x needs at least"):
+        lay.permute(x[: N - 1], recv)
+    pipe = binding.HostPipeline(w, cap, H, lanes=1, device=DEV)
+    idx_h, x_h, w_h = inp["topk_idx"].pin_memory(), inp["x"].pin_memory(), inp["weights"].pin_memory()
+    out_h = torch.empty((N, H), dtype=torch.bfloat16).pin_memory()
+    with pytest.raises(ValueError, match="x_host needs at least"):
+        pipe.submit(idx_h, x_h[: N - 1], w_h, out_h, expert=None)
+    with pytest.raises(ValueError, match="topk_idx_host needs at least"):
+        pipe.submit(idx_h[: N - 1], x_h, w_h, out_h, expert=None)
+    assert binding.kernel_launches() == launches
+    torch.cuda.synchronize()
+    assert lay.error() == 0
