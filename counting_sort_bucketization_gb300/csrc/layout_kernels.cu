@@ -21,11 +21,15 @@
 //
 // Two ways to run the three phases:
 //   - three kernels (count_tiles, scan_columns, rank_maps), chained with
-//     programmatic dependent launch;
+//     programmatic dependent launch: the two-call API, and the one-call build
+//     while a tile holds one chunk per warp (batches up to ~64 k pairs) or when
+//     the tiles do not all fit on the GPU at once.  The rank kernel stages and
+//     ranks its ids before its wait, overlapping the column scan;
 //   - one cooperative kernel (layout_fused_kernel) with two grid barriers,
-//     used when every tile's CTA fits on the GPU at once.  The tile's ids stay
-//     in shared memory from the count to the rank phase, and two launches and
-//     their gaps disappear.  Its barrier waits are bounded (MOE_ERR_TIMEOUT).
+//     the one-call build from two chunks per warp when every tile's CTA fits
+//     on the GPU at once.  The tile's ids stay in shared memory from the count
+//     to the rank phase, and two launches and their gaps disappear.  Its
+//     barrier waits are bounded (MOE_ERR_TIMEOUT).
 #include <cuda_runtime.h>
 
 #include <atomic>
