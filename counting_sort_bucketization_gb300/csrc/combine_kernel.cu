@@ -18,7 +18,6 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <mutex>
 
 #include "common.cuh"
 #include "launch.h"
@@ -157,18 +156,11 @@ __global__ void __launch_bounds__(kCombineThreads)
   }
 }
 
+// Resident CTAs per SM at the largest shared-memory size a launch uses (cached per device).
 int combine_ctas_per_sm() {
-  static int occ = 0;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    const size_t smem = (sizeof(int32_t) + sizeof(float)) * kMaxTokensPerCta * MOE_MAX_TOPK;
-    if (cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-            cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, combine_kernel, kCombineThreads, smem) != cudaSuccess ||
-        occ < 1)
-      occ = 1;
-  });
-  return occ;
+  const size_t smem = (sizeof(int32_t) + sizeof(float)) * kMaxTokensPerCta * MOE_MAX_TOPK;
+  const int occ = cached_occupancy(combine_kernel, kCombineThreads, smem);
+  return occ < 1 ? 1 : occ;
 }
 
 }  // namespace
@@ -186,15 +178,12 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream) {
   // Small batches start during the previous kernel's tail (programmatic
   // dependent launch); large ones start after it: measured on GB300, the
   // overlap saved 1.2 us of a decode step and cost 26 us of a 131072-token one.
-  cudaError_t st;
-  if (small) {
-    st = launch_pdl(combine_kernel, dim3(static_cast<unsigned>(grid)), dim3(kCombineThreads), smem, stream, a,
-                    static_cast<int>(max_tokens));
-  } else {
-    combine_kernel<<<dim3(static_cast<unsigned>(grid)), dim3(kCombineThreads), smem, stream>>>(
-        a, static_cast<int>(max_tokens));
-    st = cudaGetLastError();
-  }
+  // Both go through cudaLaunchKernelEx, whose status is this launch's own
+  // (an error left over from an earlier runtime call is not picked up).
+  const cudaError_t st = small ? launch_pdl(combine_kernel, dim3(static_cast<unsigned>(grid)), dim3(kCombineThreads),
+                                            smem, stream, a, static_cast<int>(max_tokens))
+                               : launch_plain(combine_kernel, dim3(static_cast<unsigned>(grid)),
+                                              dim3(kCombineThreads), smem, stream, a, static_cast<int>(max_tokens));
   if (st != cudaSuccess) return st;
   count_launch();
   return cudaSuccess;

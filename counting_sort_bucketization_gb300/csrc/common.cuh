@@ -101,10 +101,29 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// An ordinary launch (no attributes) through cudaLaunchKernelEx.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_plain(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                         Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // First error wins; later ones are dropped.
 __device__ __forceinline__ void set_error(int* err, int code) { atomicCAS(err, 0, code); }
 
 // Counter behind moe_kernel_launches().
 void count_launch(int n = 1);
+
+// MOE_OK for cudaSuccess; otherwise records `e` as this thread's last CUDA
+// error (moe_last_cuda_error) and returns MOE_ERR_CUDA.  Every MOE_ERR_CUDA
+// the library returns goes through it.
+int cuda_status(cudaError_t e);
 
 }  // namespace moe

@@ -60,15 +60,17 @@ extern "C" int moe_dispatch_from_host(const moe_layout_desc* desc, const int64_t
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaStream_t cs = static_cast<cudaStream_t>(copy_stream);
   CallEvent e;
-  if (e.st != cudaSuccess) return MOE_ERR_CUDA;
+  if (e.st != cudaSuccess) return moe::cuda_status(e.st);
   // The staging buffers may still be read by earlier work on `stream`.
-  if (order_after(e.ev, s, cs) != cudaSuccess) return MOE_ERR_CUDA;
-  if (N > 0 && cudaMemcpyAsync(topk_idx, topk_idx_host, sizeof(int64_t) * N * K, cudaMemcpyHostToDevice, s) !=
-                   cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (weights != nullptr && N > 0 &&
-      cudaMemcpyAsync(weights, weights_host, sizeof(float) * N * K, cudaMemcpyHostToDevice, cs) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  if (cudaError_t ce = order_after(e.ev, s, cs)) return moe::cuda_status(ce);
+  if (N > 0) {
+    if (cudaError_t ce = cudaMemcpyAsync(topk_idx, topk_idx_host, sizeof(int64_t) * N * K, cudaMemcpyHostToDevice, s))
+      return moe::cuda_status(ce);
+  }
+  if (weights != nullptr && N > 0) {
+    if (cudaError_t ce = cudaMemcpyAsync(weights, weights_host, sizeof(float) * N * K, cudaMemcpyHostToDevice, cs))
+      return moe::cuda_status(ce);
+  }
   if (int st = moe_layout_build(desc, topk_idx, expert_count, rank_count, workspace, workspace_bytes, expert_offset,
                                 rank_psum, dst_slot, src_idx, capacity_rows, total_rows, stream))
     return st;
@@ -78,15 +80,16 @@ extern "C" int moe_dispatch_from_host(const moe_layout_desc* desc, const int64_t
     if (n > 0) {
       const uint8_t* xh = static_cast<const uint8_t*>(x_host) + t0 * row_bytes;
       uint8_t* xd = static_cast<uint8_t*>(x) + t0 * row_bytes;
-      if (cudaMemcpyAsync(xd, xh, static_cast<size_t>(n * row_bytes), cudaMemcpyHostToDevice, cs) != cudaSuccess)
-        return MOE_ERR_CUDA;
-      if (sf != nullptr &&
-          cudaMemcpyAsync(static_cast<uint8_t*>(sf) + t0 * sf_row_bytes,
-                          static_cast<const uint8_t*>(sf_host) + t0 * sf_row_bytes,
-                          static_cast<size_t>(n * sf_row_bytes), cudaMemcpyHostToDevice, cs) != cudaSuccess)
-        return MOE_ERR_CUDA;
+      if (cudaError_t ce = cudaMemcpyAsync(xd, xh, static_cast<size_t>(n * row_bytes), cudaMemcpyHostToDevice, cs))
+        return moe::cuda_status(ce);
+      if (sf != nullptr) {
+        if (cudaError_t ce = cudaMemcpyAsync(static_cast<uint8_t*>(sf) + t0 * sf_row_bytes,
+                                             static_cast<const uint8_t*>(sf_host) + t0 * sf_row_bytes,
+                                             static_cast<size_t>(n * sf_row_bytes), cudaMemcpyHostToDevice, cs))
+          return moe::cuda_status(ce);
+      }
     }
-    if (order_after(e.ev, cs, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaError_t ce = order_after(e.ev, cs, s)) return moe::cuda_status(ce);
     moe_layout_desc part = *desc;
     part.num_tokens = n;
     // The first chunk's launch also zero-fills every gap row of the buffer.
@@ -115,9 +118,9 @@ extern "C" int moe_combine_to_host(const moe_layout_desc* desc, const void* expe
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaStream_t cs = static_cast<cudaStream_t>(copy_stream);
   CallEvent e;
-  if (e.st != cudaSuccess) return MOE_ERR_CUDA;
+  if (e.st != cudaSuccess) return moe::cuda_status(e.st);
   // The host buffer may still be the target of earlier copies on copy_stream.
-  if (order_after(e.ev, cs, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaError_t ce = order_after(e.ev, cs, s)) return moe::cuda_status(ce);
   const int64_t C = chunk_size(N, chunk_tokens);
   const size_t row = static_cast<size_t>(hidden) * 2;   // bf16
   for (int64_t t0 = 0; t0 < N; t0 += C) {
@@ -128,12 +131,13 @@ extern "C" int moe_combine_to_host(const moe_layout_desc* desc, const void* expe
                                        weights + t0 * K, static_cast<uint8_t*>(out) + t0 * row, workspace,
                                        workspace_bytes, stream))
       return st;
-    if (order_after(e.ev, s, cs) != cudaSuccess) return MOE_ERR_CUDA;
-    if (cudaMemcpyAsync(static_cast<uint8_t*>(out_host) + t0 * row, static_cast<uint8_t*>(out) + t0 * row,
-                        static_cast<size_t>(n) * row, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
-      return MOE_ERR_CUDA;
+    if (cudaError_t ce = order_after(e.ev, s, cs)) return moe::cuda_status(ce);
+    if (cudaError_t ce = cudaMemcpyAsync(static_cast<uint8_t*>(out_host) + t0 * row,
+                                         static_cast<uint8_t*>(out) + t0 * row, static_cast<size_t>(n) * row,
+                                         cudaMemcpyDeviceToHost, cs))
+      return moe::cuda_status(ce);
   }
   // Work enqueued on `stream` afterwards (or a synchronize of it) sees the copies done.
-  if (order_after(e.ev, cs, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaError_t ce = order_after(e.ev, cs, s)) return moe::cuda_status(ce);
   return MOE_OK;
 }

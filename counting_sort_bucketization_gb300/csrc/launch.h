@@ -109,4 +109,27 @@ WaitConfig wait_config();
 // Streaming multiprocessors of the current device (cached per device).
 int device_sm_count();
 
+// Host-side launch settings, looked up once instead of on every call.
+//   ensure_smem_limit: raise `func`'s dynamic shared-memory limit to at least
+//     `smem` bytes in the current context; the runtime call is made only when
+//     the limit must grow (cached per context, so a context created after a
+//     device reset sets it again).
+//   cached_occupancy: resident CTAs per SM of `func` at (threads, smem) on
+//     the current device, 0 if the query failed (then not cached).
+//   cooperative_launch_supported: the current device's attribute, cached.
+//   current_context_id: a nonzero identity of the current context, 0 if none.
+cudaError_t ensure_smem_limit(const void* func, size_t smem);
+int cached_occupancy(const void* func, int threads, size_t smem);
+bool cooperative_launch_supported();
+uint64_t current_context_id();
+
+template <typename... KArgs>
+cudaError_t ensure_smem_limit(void (*func)(KArgs...), size_t smem) {
+  return ensure_smem_limit(reinterpret_cast<const void*>(func), smem);
+}
+template <typename... KArgs>
+int cached_occupancy(void (*func)(KArgs...), int threads, size_t smem) {
+  return cached_occupancy(reinterpret_cast<const void*>(func), threads, smem);
+}
+
 }  // namespace moe

@@ -607,19 +607,12 @@ size_t fused_smem_bytes(const moe_layout_desc& d, const TilePlan& p) {
   return sizeof(int) * (2 * pairs + kLayoutWarps * E + 2 * E + 1 + d.num_ranks);
 }
 
-// Whether every tile's CTA of the fused kernel can be resident at once.
+// Whether every tile's CTA of the fused kernel can be resident at once
+// (device attribute and occupancy cached per device and size).
 template <typename IdT>
 bool fused_fits(const TilePlan& p, size_t smem) {
-  int dev = 0, coop = 0, per_sm = 0;
-  if (p.tiles < 1) return false;
-  if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop) return false;
-  if (cudaFuncSetAttribute(layout_fused_kernel<IdT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) != cudaSuccess)
-    return false;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layout_fused_kernel<IdT>, kLayoutThreads, smem) !=
-      cudaSuccess)
-    return false;
+  if (p.tiles < 1 || !cooperative_launch_supported()) return false;
+  const int per_sm = cached_occupancy(layout_fused_kernel<IdT>, kLayoutThreads, smem);
   return p.tiles <= static_cast<int64_t>(per_sm) * device_sm_count();
 }
 
@@ -667,8 +660,7 @@ template <typename IdT>
 cudaError_t launch_count_t(const moe_layout_desc& d, const TilePlan& p, const IdT* topk_idx, int32_t* expert_count,
                            int32_t* rank_count, int* err, int32_t* hist, int32_t* rhist, cudaStream_t stream) {
   const size_t smem1 = count_smem_bytes(d, p);
-  cudaError_t st = cudaFuncSetAttribute(count_tiles_kernel<IdT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(smem1));
+  cudaError_t st = ensure_smem_limit(count_tiles_kernel<IdT>, smem1);
   if (st != cudaSuccess) return st;
   if (p.tiles > 0) {
     st = launch_pdl(count_tiles_kernel<IdT>, dim3(static_cast<unsigned>(p.tiles)), dim3(kLayoutThreads), smem1,
@@ -688,8 +680,7 @@ template <typename IdT>
 cudaError_t launch_rank_t(const moe_layout_desc& d, const TilePlan& p, const IdT* topk_idx, const RankArgs& a,
                           cudaStream_t stream) {
   const size_t smem = rank_smem_bytes(d, p);
-  cudaError_t st = cudaFuncSetAttribute(rank_maps_kernel<IdT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(smem));
+  cudaError_t st = ensure_smem_limit(rank_maps_kernel<IdT>, smem);
   if (st != cudaSuccess) return st;
   const int64_t grid = p.tiles > 0 ? p.tiles : 1;
   st = launch_pdl(rank_maps_kernel<IdT>, dim3(static_cast<unsigned>(grid)), dim3(kLayoutThreads), smem, stream,
@@ -705,8 +696,7 @@ cudaError_t launch_rank_rows_t(const moe_layout_desc& d, const TilePlan& p, cons
   const size_t smem = sizeof(int) * (static_cast<size_t>(d.num_ranks) + 1 +
                                      static_cast<size_t>(kLayoutWarps) * d.num_ranks +
                                      2 * static_cast<size_t>(p.tile_tokens) * d.topk);
-  cudaError_t st = cudaFuncSetAttribute(rank_rows_kernel<IdT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(smem));
+  cudaError_t st = ensure_smem_limit(rank_rows_kernel<IdT>, smem);
   if (st != cudaSuccess) return st;
   const int64_t grid = p.tiles > 0 ? p.tiles : 1;
   st = launch_pdl(rank_rows_kernel<IdT>, dim3(static_cast<unsigned>(grid)), dim3(kLayoutThreads), smem, stream,
@@ -737,6 +727,7 @@ cudaError_t launch_build_t(const moe_layout_desc& d, const TilePlan& p, const Id
     if (st != cudaSuccess) return st;
     return launch_rank_t(d, p, topk_idx, a, stream);
   }
+  if (cudaError_t st = ensure_smem_limit(layout_fused_kernel<IdT>, smem)) return st;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.tiles));
   cfg.blockDim = dim3(kLayoutThreads);

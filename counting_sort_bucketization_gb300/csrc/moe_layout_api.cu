@@ -1,6 +1,7 @@
 // moe_layout_api.cu -- the extern "C" entry points of libmoe_layout.so:
 // argument checks, workspace carving and kernel launches.  Semantics and
 // error behaviour of each call are documented in include/moe_layout.h.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -30,6 +31,117 @@ int device_sm_count() {
     cache[dev] = n;
   }
   return cache[dev];
+}
+
+thread_local int t_last_cuda_error = 0;
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  t_last_cuda_error = static_cast<int>(e);
+  return MOE_ERR_CUDA;
+}
+
+// Identity of the calling thread's current CUDA context: cuCtxGetId of
+// cuCtxGetCurrent, both reached through the runtime's driver entry points (no
+// link-time dependency on the driver library).  0 when there is no current
+// context yet or the driver lacks the calls; callers then skip their caches.
+uint64_t current_context_id() {
+  using GetCurrentFn = CUresult (*)(CUcontext*);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(f);
+  });
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return static_cast<uint64_t>(id) + 1;   // never 0 for a real context
+}
+
+namespace {
+struct SmemLimit {
+  uint64_t ctx;
+  const void* func;
+  size_t bytes;
+};
+std::mutex g_smem_mu;
+std::vector<SmemLimit> g_smem_limits;
+}  // namespace
+
+cudaError_t ensure_smem_limit(const void* func, size_t smem) {
+  // Launches within the default 48 KB need no attribute.
+  if (smem <= 48 * 1024) return cudaSuccess;
+  const uint64_t ctx = current_context_id();
+  if (ctx != 0) {
+    std::lock_guard<std::mutex> lock(g_smem_mu);
+    for (const SmemLimit& l : g_smem_limits)
+      if (l.ctx == ctx && l.func == func && l.bytes >= smem) return cudaSuccess;
+  }
+  const cudaError_t st = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (st != cudaSuccess || ctx == 0) return st;
+  std::lock_guard<std::mutex> lock(g_smem_mu);
+  for (SmemLimit& l : g_smem_limits)
+    if (l.ctx == ctx && l.func == func) {
+      if (smem > l.bytes) l.bytes = smem;
+      return cudaSuccess;
+    }
+  g_smem_limits.push_back(SmemLimit{ctx, func, smem});
+  return cudaSuccess;
+}
+
+namespace {
+struct Occupancy {
+  int dev;
+  const void* func;
+  int threads;
+  size_t smem;
+  int ctas;
+};
+std::mutex g_occ_mu;
+std::vector<Occupancy> g_occ;
+}  // namespace
+
+int cached_occupancy(const void* func, int threads, size_t smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  {
+    std::lock_guard<std::mutex> lock(g_occ_mu);
+    for (const Occupancy& o : g_occ)
+      if (o.dev == dev && o.func == func && o.threads == threads && o.smem == smem) return o.ctas;
+  }
+  int n = 0;
+  if (ensure_smem_limit(func, smem) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, threads, smem) != cudaSuccess)
+    return 0;   // not cached: the next call asks again
+  std::lock_guard<std::mutex> lock(g_occ_mu);
+  if (g_occ.size() < 256) g_occ.push_back(Occupancy{dev, func, threads, smem, n});
+  return n;
+}
+
+bool cooperative_launch_supported() {
+  static std::mutex mu;
+  static std::vector<int> cache;   // per device: 0 unknown, 1 no, 2 yes
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= static_cast<int>(cache.size())) cache.resize(dev + 1, 0);
+  if (cache[dev] == 0) {
+    int coop = 0;
+    if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess) return false;
+    cache[dev] = coop ? 2 : 1;
+  }
+  return cache[dev] == 2;
 }
 
 static std::atomic<uint64_t> g_wait_limit_ns{kWaitLimitNs};
@@ -64,14 +176,6 @@ int check_workspace(const moe_layout_desc* d, const void* ws, size_t ws_bytes, W
   if (ws == nullptr || !aligned(ws, 256) || ws_bytes < w.bytes) return MOE_ERR_INVALID_ARG;
   *out = w;
   return MOE_OK;
-}
-
-thread_local int t_last_cuda_error = 0;
-
-int cuda_status(cudaError_t e) {
-  if (e == cudaSuccess) return MOE_OK;
-  t_last_cuda_error = static_cast<int>(e);
-  return MOE_ERR_CUDA;
 }
 
 template <typename T>
@@ -323,7 +427,7 @@ int moe_layout_get_error(void* workspace, int32_t* device_error, void* stream) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_status(e);
   *device_error = host;
   return MOE_OK;
 }

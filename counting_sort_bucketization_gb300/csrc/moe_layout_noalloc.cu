@@ -15,6 +15,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "launch.h"
 
 namespace moe {
 namespace {
@@ -24,23 +25,39 @@ namespace {
 // share it.
 __device__ __align__(256) unsigned char g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
 
+// Device address of the scratch in each CUDA context seen so far.
+struct ScratchAddr {
+  uint64_t ctx;   // current_context_id() of the context
+  void* ptr;
+};
 std::mutex g_scratch_mu;
-std::vector<void*> g_scratch_addr;   // per device; nullptr until that device is set up
+std::vector<ScratchAddr> g_scratch_addr;
 
-// Device address of the scratch on the current device.  The first call on a
-// device looks it up (cudaGetSymbolAddress, with that device current) and
-// caches it; later calls only read the cache.
+// Device address of the scratch in the current context.  The first call in a
+// context (the first on a device, and again the first after a device reset
+// has replaced that device's context) looks it up with cudaGetSymbolAddress,
+// with that device current, and caches it; later calls only read the cache.
 int scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (dev >= static_cast<int>(g_scratch_addr.size())) g_scratch_addr.resize(dev + 1, nullptr);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+  const uint64_t ctx = current_context_id();
+  if (ctx != 0) {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    for (const ScratchAddr& a : g_scratch_addr)
+      if (a.ctx == ctx) {
+        *out = a.ptr;
+        return MOE_OK;
+      }
   }
-  *out = g_scratch_addr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (p == nullptr) return cuda_status(cudaErrorInvalidSymbol);
+  // With no context current before the lookup (ctx == 0) the lookup made one;
+  // the next call caches its address.
+  if (ctx != 0) {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    g_scratch_addr.push_back(ScratchAddr{ctx, p});
+  }
+  *out = p;
   return MOE_OK;
 }
 
@@ -61,12 +78,12 @@ extern "C" int moe_layout_build_noalloc(const moe_layout_desc* desc, const int64
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The error word and the grid-barrier words must start at zero; the
   // histograms are rewritten in full by every call.
-  if (cudaMemsetAsync(scratch, 0, 256, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaError_t e = cudaMemsetAsync(scratch, 0, 256, s)) return moe::cuda_status(e);
   if (int st = moe_layout_build(desc, topk_idx, expert_count, rank_count, scratch, need, expert_offset, rank_psum,
                                 dst_slot, src_idx, capacity_rows, total_rows, stream))
     return st;
   // This call's device-side status: the scratch's error word.
-  if (cudaMemcpyAsync(device_error, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  if (cudaError_t e = cudaMemcpyAsync(device_error, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice, s))
+    return moe::cuda_status(e);
   return MOE_OK;
 }

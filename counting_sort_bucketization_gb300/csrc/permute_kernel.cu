@@ -32,7 +32,6 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <mutex>
 
 #include "common.cuh"
 #include "launch.h"
@@ -623,31 +622,8 @@ DynPlan make_dyn_plan(const PermuteArgs& a, int pieces) {
 
 // CTAs of the dynamic kernel resident per SM at this shared-memory size (cached).
 int dyn_ctas_per_sm(size_t smem) {
-  static std::mutex mu;
-  constexpr int kSlots = 32;
-  static size_t cached_smem[kSlots] = {};
-  static int cached_occ[kSlots] = {};
-  static int cached_dev[kSlots] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-  std::lock_guard<std::mutex> lock(mu);
-  for (int i = 0; i < kSlots; ++i)
-    if (cached_occ[i] > 0 && cached_smem[i] == smem && cached_dev[i] == dev) return cached_occ[i];
-  int occ = 0;
-  // The occupancy of a size above 48 KB counts only once the kernel may use it.
-  if (cudaFuncSetAttribute(permute_dyn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-          cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, permute_dyn_kernel, kPermuteThreads, smem) != cudaSuccess ||
-      occ < 1)
-    occ = 1;
-  for (int i = 0; i < kSlots; ++i)
-    if (cached_occ[i] == 0) {
-      cached_smem[i] = smem;
-      cached_occ[i] = occ;
-      cached_dev[i] = dev;
-      break;
-    }
-  return occ;
+  const int occ = cached_occupancy(permute_dyn_kernel, kPermuteThreads, smem);
+  return occ < 1 ? 1 : occ;
 }
 
 }  // namespace
@@ -670,8 +646,7 @@ cudaError_t launch_permute(const PermuteArgs& args, cudaStream_t stream) {
       p = make_dyn_plan(a, pieces);
       resident = static_cast<int64_t>(ctas_per_sm(p.smem)) * device_sm_count();
     }
-    cudaError_t st = cudaFuncSetAttribute(permute_dyn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          static_cast<int>(p.smem));
+    cudaError_t st = ensure_smem_limit(permute_dyn_kernel, p.smem);
     if (st != cudaSuccess) return st;
     p.grid = max64(1, min64(resident, a.num_tokens * p.pieces));
     st = launch_pdl(permute_dyn_kernel, dim3(static_cast<unsigned>(p.grid)), dim3(kPermuteThreads), p.smem, stream,
@@ -681,8 +656,7 @@ cudaError_t launch_permute(const PermuteArgs& args, cudaStream_t stream) {
     return cudaSuccess;
   }
   const PermutePlan p = make_permute_plan(a, device_sm_count());
-  cudaError_t st = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(p.smem));
+  cudaError_t st = ensure_smem_limit(permute_kernel, p.smem);
   if (st != cudaSuccess) return st;
   st = launch_pdl(permute_kernel, dim3(static_cast<unsigned>(p.grid)), dim3(kPermuteThreads), p.smem, stream, a, p);
   if (st != cudaSuccess) return st;

@@ -31,8 +31,6 @@
 // 128-byte run of the output column.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "common.cuh"
 #include "launch.h"
 #include "ptx.cuh"
@@ -180,23 +178,11 @@ size_t sf_smem_bytes(int64_t cols) {
 }
 
 // Resident CTAs per SM of one kernel variant at a given dynamic shared-memory
-// size (cached; at most kSfPassCols sizes per variant exist).
+// size (cached per device).
 int sf_ctas_per_sm(bool vec, size_t smem) {
-  static std::mutex mu;
-  static int cached[2][kSfPassCols + 1][8] = {};   // [variant][columns in a pass][device]
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 8) return 1;
-  const size_t cols = smem / (kSfLine * sizeof(uint32_t));
-  std::lock_guard<std::mutex> lock(mu);
-  int& occ = cached[vec ? 1 : 0][cols][dev];
-  if (occ == 0) {
-    int v = 0;
-    const cudaError_t st =
-        vec ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, sf_col_major_kernel<true>, kSfThreads, smem)
-            : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, sf_col_major_kernel<false>, kSfThreads, smem);
-    occ = (st == cudaSuccess && v >= 1) ? v : 1;
-  }
-  return occ;
+  const int occ = vec ? cached_occupancy(sf_col_major_kernel<true>, kSfThreads, smem)
+                      : cached_occupancy(sf_col_major_kernel<false>, kSfThreads, smem);
+  return occ < 1 ? 1 : occ;
 }
 
 }  // namespace

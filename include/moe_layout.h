@@ -283,8 +283,10 @@ MOE_API int moe_combine_unpermute(const moe_layout_desc* desc, const void* exper
  *  - Problems whose workspace (moe_layout_workspace_bytes) is larger than
  *    that are rejected with MOE_ERR_UNSUPPORTED before anything is launched.
  *  - The first call on a device looks up the array's device address (with
- *    that device current) and caches it; make that first call before any
- *    stream capture.
+ *    that device current) and caches it for that device's CUDA context; make
+ *    that first call before any stream capture.  After a device reset the
+ *    device has a new context and the array may sit at a new address: the
+ *    first call in the new context looks it up again (again outside capture).
  *  - Every call on a device shares the array.  Each call clears the parts
  *    that must start at zero, but calls that overlap on the GPU (different
  *    streams, no ordering between them) race on it and give wrong results.
@@ -379,8 +381,9 @@ MOE_API int moe_debug_set_waits(uint64_t limit_ns, uint32_t barrier_extra, uint3
 
 /*
  * The CUDA error code (cudaError_t) behind this thread's most recent
- * MOE_ERR_CUDA, or 0 if there was none; *message (if non-NULL) receives its
- * description.  Diagnostics only: a status the pages do not define.
+ * MOE_ERR_CUDA from any entry point, or 0 if there was none; *message (if
+ * non-NULL) receives its description.  Diagnostics only: a status the pages
+ * do not define.
  */
 MOE_API int moe_last_cuda_error(const char** message);
 

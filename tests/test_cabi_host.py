@@ -141,3 +141,65 @@ def test_strerror_and_launch_counter(lib):
         assert lib.moe_strerror(code)
     assert lib.moe_strerror(99) == b"unknown status"
     assert lib.moe_kernel_launches() >= 0
+
+
+def _no_cuda_device() -> bool:
+    try:
+        import torch
+        return not torch.cuda.is_available()
+    except Exception:  # pragma: no cover
+        return True
+
+
+@pytest.mark.skipif(not _no_cuda_device(), reason="needs a machine without a CUDA device (fake pointers below)")
+def test_every_cuda_failure_is_recorded_for_last_cuda_error(lib):
+    """On a machine with no CUDA device the first CUDA call of each entry point
+    fails; every one of them must return MOE_ERR_CUDA (2) and leave the CUDA
+    error behind it for moe_last_cuda_error, in the calling thread.  The
+    pointers are never dereferenced: each path fails at its first CUDA call,
+    which cannot reach a device."""
+    import threading
+
+    import numpy as np
+
+    lib.moe_last_cuda_error.argtypes = [ctypes.POINTER(ctypes.c_char_p)]
+    lib.moe_last_cuda_error.restype = ctypes.c_int
+    p, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    lib.moe_layout_build_noalloc.argtypes = [ctypes.POINTER(binding._CDesc), p, p, p, p, p, p, p, i64, p, p, p]
+    lib.moe_layout_build_noalloc.restype = ctypes.c_int
+    N, K, E, R, A, H = 64, 8, 16, 4, 4, 16
+    d = ctypes.byref(_desc(N, K, E, R, A))
+    n = ctypes.c_size_t(0)
+    assert lib.moe_layout_workspace_bytes(d, ctypes.byref(n)) == 0
+    fake = ctypes.c_void_p(1 << 20)
+    ids = np.zeros((N, K), np.int64)
+    x = np.zeros((N, H), np.uint16)
+    w = np.zeros((N, K), np.float32)
+    host = lambda a: ctypes.c_void_p(a.ctypes.data)
+    calls = {
+        "moe_dispatch_from_host": lambda: lib.moe_dispatch_from_host(
+            d, host(ids), host(x), 2 * H, None, 0, host(w), fake, fake, None, fake, fake, fake, fake, fake, fake,
+            fake, fake, fake, None, 1024, fake, n.value, 0, None, fake),
+        "moe_combine_to_host": lambda: lib.moe_combine_to_host(
+            d, fake, 1024, H, fake, fake, fake, host(x), fake, n.value, 0, None, fake),
+        "moe_layout_build_noalloc": lambda: lib.moe_layout_build_noalloc(
+            d, fake, fake, fake, fake, fake, fake, fake, 1024, fake, fake, None),
+        "moe_layout_build": lambda: lib.moe_layout_build(
+            d, fake, fake, fake, fake, n.value, fake, fake, fake, fake, 1024, fake, None),
+        "moe_layout_get_error": lambda: lib.moe_layout_get_error(fake, ctypes.byref(ctypes.c_int32()), None),
+    }
+    results = {}
+
+    def run():
+        for name, call in calls.items():
+            st = call()
+            results[name] = (st, lib.moe_last_cuda_error(None))
+
+    t = threading.Thread(target=run)
+    t.start()
+    t.join()
+    for name, (st, code) in results.items():
+        assert st == 2, f"{name} returned {st}"
+        assert code != 0, f"{name}: moe_last_cuda_error() is 0 after MOE_ERR_CUDA"
+    # The record is per thread: this thread has had no failing CUDA call.
+    assert lib.moe_last_cuda_error(None) == 0

@@ -10,8 +10,7 @@ import ctypes
 import numpy as np
 import pytest
 
-hyp = pytest.importorskip("hypothesis")
-from hypothesis import HealthCheck, given, settings, strategies as st  # noqa: E402
+from hypothesis import HealthCheck, given, settings, strategies as st  # noqa: E402  (conftest skips the module without it)
 
 import oracle  # noqa: E402
 import oracle_checks as oc  # noqa: E402
