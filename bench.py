@@ -1,12 +1,16 @@
 """Benchmark of the MoE dispatch layout hot path on GB300.
 
 One step = one pass of the whole path over one batch of the workload:
-count -> scan (offsets + slot maps) -> permute (expand-mode row scatter with
-zero padding) -> combine (weighted top-k gather back to token order), each a
-launch of this library through its C ABI.  Prints ONE JSON line.
+layout (count -> aligned prefix sums -> slot maps) -> permute (expand-mode
+row scatter with zero padding) -> combine (weighted top-k gather back to
+token order), each a launch of this library through its C ABI.  Prints ONE
+JSON line.  The default workload is the largest single-GPU one, round-trip
+(131072 tokens, top-8 of 384 experts, hidden 4096 bf16); the line also
+carries a clocked entry for every other large workload (``per_config``).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload roundtrip]
     python bench.py --impl reference ...   # the CPU oracle as the reference arm
+    python bench.py --profile --workload roundtrip --tokens 16384 ...   # small footprint, for ncu
 
 Multi-GPU (torchrun, one process per GPU): replicas.  Logical ranks are
 partitions of one GPU's buffer, so there is no data-path collective; each
@@ -15,6 +19,7 @@ process runs its own batch (weak scaling) and timing is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -23,6 +28,7 @@ import statistics
 import subprocess
 import sys
 import tempfile
+import threading
 import time
 
 import numpy as np
@@ -38,19 +44,48 @@ METRIC = "MoE dispatch permute tokens/s and achieved HBM GB/s vs GB300 peak (1 G
 UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20          # > 2x the 129 MB L2
+DEFAULT_WORKLOAD = "roundtrip"      # the largest workload that fits one GPU
 
-# DRAM traffic of the permute kernel from ncu captures (dram__bytes_read.sum +
-# dram__bytes_write.sum) per launch, by workload and layout mode, tied to the
-# kernel sources they were measured on.  bench reports null if they changed
-# or the workload was not captured.
-PERMUTE_TRAFFIC = {"sha256": "84d1af49c0472e56db817dec3fd9e137f27bff7bb16289179472e7b8226b4aae",
-                   "bytes_per_launch": {"decode": 58_915_840 + 646_384_640,
-                                        "decode/non-expand": 58_925_568 + 249_672_704,
-                                        "skewed": 235_471_616 + 1_841_223_936,
-                                        "prefill_fp8": 243_337_984 + 1_997_432_064}}
-PERMUTE_SOURCES = ["counting_sort_bucketization_gb300/csrc/permute_kernel.cu",
-                   "counting_sort_bucketization_gb300/csrc/ptx.cuh",
-                   "counting_sort_bucketization_gb300/csrc/common.cuh"]
+# DRAM traffic per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum,
+# one metric pass) of each HBM-bound kernel, by workload, tied to the sources
+# it was measured on: a kernel whose sources changed since reports null.  How
+# each figure was taken is in profiles/traffic_by_kernel_and_workload.md.
+TRAFFIC = {
+    "permute_dyn_kernel": {
+        "sources": ["counting_sort_bucketization_gb300/csrc/permute_kernel.cu",
+                    "counting_sort_bucketization_gb300/csrc/ptx.cuh",
+                    "counting_sort_bucketization_gb300/csrc/common.cuh"],
+        "sha256": None,
+        "bytes_per_launch": {},
+    },
+    "combine_kernel": {
+        "sources": ["counting_sort_bucketization_gb300/csrc/combine_kernel.cu",
+                    "counting_sort_bucketization_gb300/csrc/ptx.cuh",
+                    "counting_sort_bucketization_gb300/csrc/common.cuh"],
+        "sha256": None,
+        "bytes_per_launch": {},
+    },
+    "sf_col_major_kernel": {
+        "sources": ["counting_sort_bucketization_gb300/csrc/sf_layout_kernel.cu",
+                    "counting_sort_bucketization_gb300/csrc/ptx.cuh",
+                    "counting_sort_bucketization_gb300/csrc/common.cuh"],
+        "sha256": None,
+        "bytes_per_launch": {},
+    },
+}
+
+# Kernels behind each stage of a step (the layout's depend on the batch size).
+STAGE_KERNEL = {"permute": "permute_dyn_kernel", "permute_ranks": "permute_dyn_kernel",
+                "combine": "combine_kernel", "sf_col_major": "sf_col_major_kernel",
+                "layout": "count_tiles + scan_columns + rank_maps, or layout_fused_kernel",
+                "rank_rows": "rank_rows_kernel"}
+HBM_STAGES = ("permute", "permute_ranks", "combine", "sf_col_major")
+
+# The other large workloads, each with a short clocked loop of its own in the
+# default run: (key, workload, layout mode).
+PER_CONFIG = [("decode", "decode", {}), ("skewed", "skewed", {}), ("prefill_fp8", "prefill_fp8", {}),
+              ("decode/non-expand", "decode", {"non_expand": True}),
+              ("prefill_fp8/sf-col-major", "prefill_fp8", {"sf_col_major": True})]
 
 
 # ---------------------------------------------------------------- helpers
@@ -72,6 +107,19 @@ def sources_sha256(paths) -> str:
         with open(os.path.join(REPO, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
+
+
+def traffic_of(kernel: str, key: str):
+    """(bytes per launch, how it was taken) for a kernel on a workload, or (None, why not)."""
+    t = TRAFFIC.get(kernel)
+    if t is None:
+        return None, "not an HBM-bound kernel"
+    entry = t["bytes_per_launch"].get(key)
+    if entry is None:
+        return None, "not captured on this workload"
+    if t["sha256"] != sources_sha256(t["sources"]):
+        return None, "sources changed since the capture"
+    return entry["bytes"], entry["how"]
 
 
 def dist_env():
@@ -117,59 +165,128 @@ def config_of(w: wl.Workload) -> dict:
                   "256 MiB buffer read, so each step starts with a cold L2 holding no dirty lines"}
 
 
+# ----------------------------------------------------------------- clocks
+_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+            0x80: "hw_power_brake_slowdown"}
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 100 ms while running."""
+    """SM clock, its maximum, power and clock-event (throttle) reasons of one
+    GPU, sampled every ``period_s`` by a background thread through NVML (read
+    only), with ``nvidia-smi -lms 100`` as the fallback when NVML cannot be
+    loaded.  ``window(t0, t1)`` summarises the samples taken between two
+    ``time.perf_counter()`` readings."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    def __init__(self, device_index: int, period_s: float = 0.005):
+        self.period = period_s
+        self.samples = []            # (perf_counter, sm_mhz, sm_max_mhz, reasons mask, power W)
+        self.source = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._smi = None
+        self._nvml = None
+        self._handle = None
+        self._index = device_index
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.file = None
-
-    def __enter__(self):
+    # -- NVML through ctypes (no Python package needed)
+    def _open_nvml(self) -> bool:
         try:
-            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
-                 "-i", str(self.gpu)], stdout=self.file, stderr=subprocess.DEVNULL)
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return False
+        if lib.nvmlInit_v2() != 0:
+            return False
+        handle = ctypes.c_void_p()
+        found = False
+        try:   # the CUDA device's PCI address, so that CUDA_VISIBLE_DEVICES cannot mislead the index
+            p = torch.cuda.get_device_properties(self._index)
+            bus = f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0".encode()
+            found = lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(handle)) == 0
+        except (AttributeError, RuntimeError):
+            found = False
+        if not found and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self._index), ctypes.byref(handle)) != 0:
+            return False
+        self._nvml, self._handle = lib, handle
+        try:
+            self._reasons_fn = lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self._reasons_fn = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return True
+
+    def _poll_nvml(self):
+        lib, h = self._nvml, self._handle
+        sm, mx, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            t = time.perf_counter()
+            ok = lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0      # NVML_CLOCK_SM
+            ok = ok and lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0
+            ok = ok and self._reasons_fn(h, ctypes.byref(rs)) == 0
+            power = pw.value / 1e3 if lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) == 0 else None
+            if ok:
+                self.samples.append((t, float(sm.value), float(mx.value), int(rs.value), power))
+            self._stop.wait(self.period)
+
+    def start(self):
+        if self._open_nvml():
+            self.source = f"nvml every {self.period * 1e3:.0f} ms"
+            self._thread = threading.Thread(target=self._poll_nvml, daemon=True)
+            self._thread.start()
+            return self
+        fields = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_power_cap")
+        try:
+            self._file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self._smi = subprocess.Popen(["nvidia-smi", f"--query-gpu={fields}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self._index)],
+                                         stdout=self._file, stderr=subprocess.DEVNULL)
+            self._smi_t0 = time.perf_counter()
+            self.source = "nvidia-smi every 100 ms"
             time.sleep(0.3)
-        except (OSError, FileNotFoundError):
-            self.proc = None
+        except OSError:
+            self._smi = None
         return self
 
-    def __exit__(self, *exc):
-        if self.proc is not None:
-            time.sleep(0.15)
-            self.proc.terminate()
+    def stop(self):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join(timeout=2)
+        if self._smi is not None:
+            self._smi.terminate()
             try:
-                self.proc.wait(timeout=5)
+                self._smi.wait(timeout=5)
             except subprocess.TimeoutExpired:
-                self.proc.kill()
+                self._smi.kill()
+            bits = (0x8, 0x40, 0x20, 0x4)
+            dt = 0.1
+            with open(self._file.name) as f:
+                for i, line in enumerate(f):
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 7:
+                        continue
+                    try:
+                        mask = sum(b for b, fl in zip(bits, parts[3:7]) if fl == "Active")
+                        self.samples.append((self._smi_t0 + i * dt, float(parts[0]), float(parts[1]), mask,
+                                             float(parts[2])))
+                    except ValueError:
+                        continue
+            os.unlink(self._file.name)
+            self._smi = None
 
-    def summary(self) -> dict | None:
-        if self.proc is None or self.file is None:
+    def window(self, t0: float, t1: float) -> dict | None:
+        if self.source is None:
             return None
-        self.file.flush()
-        rows = []
-        with open(self.file.name) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
-                except ValueError:
-                    continue
-        os.unlink(self.file.name)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, flags in rows for i, fl in enumerate(flags) if fl == "Active"})
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not inside:   # a window shorter than the period: the first sample after its start
+            after = [s for s in self.samples if s[0] >= t0]
+            inside = after[:1]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": self.source}
+        reasons = sorted({name for s in inside for bit, name in _REASONS.items() if s[3] & bit})
+        powers = [s[4] for s in inside if s[4] is not None]
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": max(s[2] for s in inside),
+                "sm_mhz_min": min(s[1] for s in inside), "reasons": reasons, "samples": len(inside),
+                "power_w_max": max(powers) if powers else None, "source": self.source}
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -235,10 +352,15 @@ class OracleRunner:
 
 # ------------------------------------------------------------ native run
 def algorithmic_bytes(w: wl.Workload, lay, sf_col_major: bool = False) -> dict:
-    """Bytes each kernel must move, from the layout of this batch.  With
-    ``sf_col_major`` the permute moves the rows only and the scale factors
-    go column-major in their own kernel (reads each routed token's scale
-    row, writes every receive row's words, reads the inverse map)."""
+    """Bytes each kernel must move, from the layout of this batch.
+
+    permute: each routed token's row (and scale row) read once, one row
+    written per valid pair and per alignment-gap row, the slots and offsets
+    read; combine: one expert-output row read per valid pair, slots and
+    weights read, one output row written per token.  With ``sf_col_major`` the
+    permute moves the rows only and the scale factors go column-major in
+    their own kernel (each routed token's scale row read, every receive row's
+    words written, the inverse map read)."""
     N, K, E = w.num_tokens, w.topk, w.num_experts
     dst = lay.dst_slot[: N * K].view(N, K)
     valid = dst >= 0
@@ -249,11 +371,313 @@ def algorithmic_bytes(w: wl.Workload, lay, sf_col_major: bool = False) -> dict:
     permute = n_tok * rb + P * rb + (rows - P) * rb + N * K * 4 + 2 * (E + 1) * 4
     sf_cm = n_tok * w.sf_row_bytes + rows * w.sf_row_bytes + rows * 4 if sf_col_major else 0
     combine = P * w.hidden * 2 + N * K * 8 + N * w.hidden * 2 if w.row_dtype == "bf16" else 0
-    count = N * K * 8
-    scan = N * K * 8 + N * K * 4 + rows * 4
-    return {"permute": permute, "combine": combine, "count": count, "scan": scan, "sf_col_major": sf_cm,
-            "P": P, "rows": rows,
-            "tokens_routed": n_tok}
+    layout = N * K * 8 + N * K * 4 + rows * 4
+    return {"permute": permute, "combine": combine, "layout": layout, "sf_col_major": sf_cm,
+            "P": P, "rows": rows, "tokens_routed": n_tok}
+
+
+class Case:
+    """One workload resident on the device, with its stages ready to run.
+
+    ``eo_alias`` makes the combine read the receive buffer itself instead of a
+    separate stand-in expert output (same rows, same bytes; only for the small
+    profiling footprint)."""
+
+    def __init__(self, w: wl.Workload, seed: int, dev, non_expand=False, sf_col_major=False, eo_alias=False,
+                 keep_inputs=False):
+        from counting_sort_bucketization_gb300 import binding
+        self.w, self.dev = w, dev
+        self.non_expand = non_expand
+        inp = wl.make(w, seed)
+        self.inp = inp if keep_inputs else None
+        N, H = w.num_tokens, w.hidden
+        cap = wl.worst_case_rows(w)
+        self.cap = cap
+        self.idx_d = inp["topk_idx"].to(dev)
+        self.x_d = inp["x"].to(dev)
+        sf_d = inp["sf"].to(dev) if inp["sf"] is not None else None
+        self.sf_d = sf_d
+        self.wt_d = inp["weights"].to(dev)
+        lay = binding.Layout(w, cap, device=dev)
+        self.lay = lay
+        self.recv = torch.empty((cap, H), dtype=self.x_d.dtype, device=dev)
+        recv_sf = torch.empty((cap, sf_d.shape[1]), dtype=sf_d.dtype, device=dev) if sf_d is not None else None
+        self.sf_cm = sf_col_major and sf_d is not None
+        recv_sf_cm = binding.new_sf_col_major(sf_d.shape[1], cap, device=dev) if self.sf_cm else None
+        perm_sf, perm_recv_sf = (None, None) if self.sf_cm else (sf_d, recv_sf)
+        self.do_combine = w.row_dtype == "bf16" and not non_expand
+        self.out = torch.empty((N, H), dtype=torch.bfloat16, device=dev) if self.do_combine else None
+        lay.build(self.idx_d)
+        lay.permute(self.x_d, self.recv, sf_d, recv_sf)
+        self.eo = None
+        if self.do_combine:
+            if eo_alias:
+                self.eo = self.recv
+            else:
+                # The round-trip stand-in expert applied once (harness, untimed): rows of
+                # expert e scaled by 1 + e/384, in pieces to bound the temporaries.
+                rows = int(lay.total_rows.item())
+                self.eo = torch.zeros((cap, H), dtype=torch.bfloat16, device=dev)
+                off = lay.expert_offset.to(torch.int64)
+                scale = inp["expert_scale"].to(dev)
+                for r0 in range(0, rows, 1 << 16):
+                    r1 = min(rows, r0 + (1 << 16))
+                    row_e = torch.searchsorted(off[1:], torch.arange(r0, r1, device=dev), right=True)
+                    self.eo[r0:r1] = (self.recv[r0:r1].float() * scale[row_e][:, None]).to(torch.bfloat16)
+        assert lay.error() == 0, "device error during set-up"
+        if non_expand:
+            ne_cap = N * w.num_ranks
+            lay.rank_rows(self.idx_d, capacity_rows=ne_cap)
+            self.recv_ne = torch.empty((ne_cap, H), dtype=self.x_d.dtype, device=dev)
+            self.recv_ne_sf = torch.empty((ne_cap, sf_d.shape[1]), dtype=sf_d.dtype, device=dev) \
+                if sf_d is not None else None
+            lay.permute_ranks(self.x_d, self.recv_ne, sf_d, self.recv_ne_sf)
+            assert lay.error() == 0, "device error during set-up"
+        # The step's kernels in order.
+        self.stages = [("layout", lambda: lay.build(self.idx_d))]
+        if non_expand:
+            self.stages += [("rank_rows", lambda: lay.rank_rows(self.idx_d, capacity_rows=ne_cap)),
+                            ("permute_ranks", lambda: lay.permute_ranks(self.x_d, self.recv_ne, sf_d,
+                                                                        self.recv_ne_sf))]
+        else:
+            self.stages.append(("permute", lambda: lay.permute(self.x_d, self.recv, perm_sf, perm_recv_sf)))
+            if self.sf_cm:
+                self.stages.append(("sf_col_major", lambda: lay.permute_sf_col_major(sf_d, recv_sf_cm)))
+            if self.do_combine:
+                self.stages.append(("combine", lambda: lay.combine(self.eo, self.wt_d, self.out)))
+        self.ab = algorithmic_bytes(w, lay, self.sf_cm)
+        if non_expand:
+            rows_ne = int(lay.rank_psum[-1].item())
+            rb_all = w.row_bytes + w.sf_row_bytes
+            # each routed token's row read once, one row written per (token, rank reached), the slots read
+            self.ab["permute_ranks"] = self.ab["tokens_routed"] * rb_all + rows_ne * rb_all + N * w.topk * 4
+            self.ab["rows_non_expand"] = rows_ne
+        self.key = w.name + ("/non-expand" if non_expand else "") + ("/sf-col-major" if self.sf_cm else "")
+
+    def run(self):
+        for _, fn in self.stages:
+            fn()
+
+
+class Flusher:
+    """Writes one 256 MiB buffer and reads another, so that the next step starts
+    with a cold L2 that holds no dirty lines."""
+
+    def __init__(self, dev):
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.max()
+
+
+def new_events(n):
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def time_case(case: Case, steps: int, warmup: int, flush: Flusher, world: int, sampler: ClockSampler | None,
+              breakdown_steps: int, enqueue_steps: int) -> dict:
+    """Warm-up, then exactly ``steps`` timed steps (one event pair around each
+    whole step, L2 flushed before it), then the per-kernel breakdown and the
+    host's enqueue time per step."""
+    from counting_sort_bucketization_gb300 import binding
+    dev, stream = case.dev, torch.cuda.current_stream(case.dev)
+
+    # One event before and one after the whole step: an event between two
+    # kernels would stand between them in the stream and stop the next one
+    # from starting during the previous one's tail (the programmatic
+    # dependent launch the kernels are built for).
+    def step(ev):
+        ev[0].record(stream)
+        case.run()
+        ev[1].record(stream)
+
+    for _ in range(warmup):
+        flush()
+        step(new_events(2))
+    torch.cuda.synchronize(dev)
+    assert case.lay.error() == 0, "device error during warm-up"
+    evs = [new_events(2) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    launches0 = binding.kernel_launches()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        flush()
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    t1 = time.perf_counter()
+    barrier(world)
+    launches = binding.kernel_launches() - launches0
+    assert case.lay.error() == 0, "device error in the timed region"
+    step_ms = np.array([e[0].elapsed_time(e[1]) for e in evs])
+    ms_per_step = reduce_max(float(step_ms.mean()), world, dev)
+
+    # Per-kernel breakdown: separate steps with an event after every kernel.
+    n_break = max(1, min(steps, breakdown_steps))
+    kevs = [new_events(len(case.stages) + 1) for _ in range(n_break)]
+    for i in range(n_break):
+        flush()
+        ev = kevs[i]
+        ev[0].record(stream)
+        for j, (_, fn) in enumerate(case.stages):
+            fn()
+            ev[j + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(len(case.stages))] for e in kevs])
+    kern_ms = dict(zip([name for name, _ in case.stages], per.mean(axis=0).tolist()))
+
+    # Host enqueue time: the calls of a step back to back with no flush, no
+    # events and no synchronisation inside the loop.
+    n_enq = max(1, min(steps, enqueue_steps))
+    torch.cuda.synchronize(dev)
+    e0 = time.perf_counter()
+    for _ in range(n_enq):
+        case.run()
+    e1 = time.perf_counter()
+    torch.cuda.synchronize(dev)
+    assert case.lay.error() == 0, "device error in the breakdown steps"
+    return {"ms_per_step": ms_per_step, "step_ms_min": float(step_ms.min()), "step_ms_max": float(step_ms.max()),
+            "kernels_ms": kern_ms, "launches": launches, "wall_s": t1 - t0,
+            "clocks": sampler.window(t0, t1) if sampler is not None else None,
+            "breakdown_steps": n_break, "host_enqueue_us_per_step": (e1 - e0) / n_enq * 1e6,
+            "host_enqueue_steps": n_enq}
+
+
+def roofline_of(case: Case, stage: str, kern_ms: dict, peak: dict) -> dict:
+    kernel = STAGE_KERNEL[stage]
+    t_s = kern_ms[stage] / 1e3
+    ab = case.ab[stage]
+    achieved = ab / t_s / 1e9
+    traffic, how = traffic_of(kernel, case.key)
+    r = {"kernel": kernel, "bound": "hbm", "achieved": achieved, "peak": peak["hbm_gbs"],
+         "peak_source": peak["source"], "unit": "GB/s", "frac": achieved / peak["hbm_gbs"], "traffic": traffic,
+         "traffic_source": how, "algorithmic_bytes_per_launch": ab, "launch_ms": kern_ms[stage]}
+    if traffic is not None:
+        r["achieved_dram"] = traffic / t_s / 1e9
+        r["frac_dram"] = r["achieved_dram"] / peak["hbm_gbs"]
+    return r
+
+
+def case_summary(case: Case, t: dict, peak: dict, world: int) -> dict:
+    """Throughput and per-kernel rooflines of one timed case."""
+    N = case.w.num_tokens
+    kern = t["kernels_ms"]
+    hbm = [s for s in HBM_STAGES if s in kern]
+    rl = {s: roofline_of(case, s, kern, peak) for s in hbm}
+    dispatch_ms = sum(v for k, v in kern.items() if k != "combine")
+    return {
+        "config": config_of(case.w), "ms_per_step": t["ms_per_step"], "tokens_per_s": world * N / (t["ms_per_step"] / 1e3),
+        "dispatch_tokens_per_s": world * N / (dispatch_ms / 1e3),
+        "kernels_ms": kern, "kernels_gbs": {s: rl[s]["achieved"] for s in hbm},
+        "kernels_frac": {s: rl[s]["frac"] for s in hbm},
+        "kernels_frac_dram": {s: rl[s].get("frac_dram") for s in hbm},
+        "rooflines": rl,
+        "layout": {"valid_pairs": case.ab["P"], "rows": case.ab["rows"], "tokens_routed": case.ab["tokens_routed"],
+                   **({"rows_non_expand": case.ab["rows_non_expand"]} if case.non_expand else {})},
+        "clocks": t["clocks"], "steps": None, "host_enqueue_us_per_step": t["host_enqueue_us_per_step"],
+    }
+
+
+def link_ceiling(h2d, d2h, reps: int, dev) -> dict:
+    """Pinned host<->device copies of exactly one step's bytes: each direction
+    alone, then both at once on two streams (the ceiling of any pipeline that
+    moves these bytes).  ``h2d`` is a list of (device dst, host src), ``d2h`` of
+    (host dst, device src)."""
+    main = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(directions):
+        # Each repetition forks the directions onto their streams and joins them again.
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(main)
+        for _ in range(reps):
+            for s, pairs in directions:
+                s.wait_stream(main)
+                with torch.cuda.stream(s):
+                    for dst, src in pairs:
+                        dst.copy_(src, non_blocking=True)
+            for s, _ in directions:
+                main.wait_stream(s)
+        b.record(main)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / reps / 1e3   # s per step
+
+    bi = sum(d.numel() * d.element_size() for d, _ in h2d)
+    bo = sum(d.numel() * d.element_size() for d, _ in d2h)
+    timed([(s_in, h2d), (s_out, d2h)])   # warm-up
+    t_in = timed([(s_in, h2d)])
+    t_out = timed([(s_out, d2h)])
+    t_both = timed([(s_in, h2d), (s_out, d2h)])
+    return {"h2d_gbs": bi / t_in / 1e9, "d2h_gbs": bo / t_out / 1e9, "both_gbs": (bi + bo) / t_both / 1e9,
+            "step_ms_both_directions": t_both * 1e3, "reps": reps}
+
+
+def run_e2e(case: Case, args, world: int, dev) -> dict:
+    """End to end through the public API with host buffers: pinned ids, rows and
+    weights in, the combined tokens back (dispatch-only workloads: the receive
+    rows back).  moe_dispatch_from_host and moe_combine_to_host overlap the
+    copies with the kernels, and HostPipeline keeps ``--e2e-lanes`` batches in
+    flight so one batch's copy back overlaps the next one's copy in.  Every
+    copy is inside the timed region; each step's working set is larger than L2."""
+    from counting_sort_bucketization_gb300 import binding
+    w, inp = case.w, case.inp
+    N, H = w.num_tokens, w.hidden
+    stream = torch.cuda.current_stream(dev)
+    idx_h = inp["topk_idx"].pin_memory()
+    x_h = inp["x"].pin_memory()
+    sf_h = inp["sf"].pin_memory() if inp["sf"] is not None else None
+    wt_h = inp["weights"].pin_memory()
+    do_combine = case.do_combine
+    out_shape, out_dtype = ((N, H), torch.bfloat16) if do_combine else ((case.cap, H), case.x_d.dtype)
+    lanes = max(1, args.e2e_lanes)
+    outs_h = [torch.empty(out_shape, dtype=out_dtype).pin_memory() for _ in range(lanes)]
+    h2d = idx_h.numel() * 8 + x_h.numel() * x_h.element_size() + wt_h.numel() * 4 + \
+        (sf_h.numel() * 4 if sf_h is not None else 0)
+    d2h = outs_h[0].numel() * outs_h[0].element_size()
+    chunk_of = lambda n_chunks: -(-N // max(1, n_chunks))
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    eo = case.eo
+    expert = (lambda lay_, recv_, recv_sf_: eo) if do_combine else None
+    sf_cols = case.sf_d.shape[1] if case.sf_d is not None else 0
+
+    def ms_per_step(n_lanes, n_chunks):
+        pipe = binding.HostPipeline(w, case.cap, H, x_dtype=case.x_d.dtype, sf_cols=sf_cols, lanes=n_lanes,
+                                    chunk_tokens=chunk_of(n_chunks), device=dev)
+        for i in range(2 * n_lanes):
+            pipe.submit(idx_h, x_h, wt_h, outs_h[i % n_lanes], expert, sf_h)
+        pipe.join(stream)
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(e2e_steps):
+            pipe.submit(idx_h, x_h, wt_h, outs_h[i % n_lanes], expert, sf_h)
+        pipe.join(stream)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        assert pipe.errors() == [0] * n_lanes, "device error in the end-to-end steps"
+        del pipe
+        torch.cuda.empty_cache()
+        return a.elapsed_time(b) / e2e_steps
+
+    step_ms = reduce_max(ms_per_step(lanes, args.e2e_chunks), world, dev)
+    # One batch in flight, its copies overlapped with the kernels in 4 chunks: the reference point.
+    one_ms = reduce_max(ms_per_step(1, 4), world, dev)
+    value = world * N / (step_ms / 1e3)
+    # The host link's own ceiling for exactly these bytes, in the same process.
+    h2d_pairs = [(case.idx_d, idx_h), (case.x_d, x_h), (case.wt_d, wt_h)] + \
+        ([(case.sf_d, sf_h)] if sf_h is not None else [])
+    d2h_src = case.out if do_combine else case.recv
+    link = link_ceiling(h2d_pairs, [(outs_h[0], d2h_src)], max(2, min(10, e2e_steps)), dev)
+    ceiling = N / (link["step_ms_both_directions"] / 1e3) * world
+    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+            "chunks": args.e2e_chunks, "batches_in_flight": lanes, "ms_per_step": step_ms,
+            "value_one_batch_in_flight_4_chunks": world * N / (one_ms / 1e3),
+            "link": link, "link_ceiling_tokens_per_s": ceiling, "frac_of_link": value / ceiling,
+            "api": "HostPipeline: moe_dispatch_from_host + moe_combine_to_host" if do_combine
+            else "HostPipeline: moe_dispatch_from_host + receive rows copied back"}
 
 
 def run_layout_only(args, local):
@@ -270,15 +694,13 @@ def run_layout_only(args, local):
     if args.ids_int32:
         idx = idx.to(torch.int32)
     lay = binding.Layout(w, wl.worst_case_rows(w), device=dev)
-    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush = Flusher(dev)
     times = {}
     # The two-call API (count, then scan) takes int64 ids only.
     for fused in ((True,) if args.ids_int32 else (True, False)):
         evs = []
         for i in range(args.warmup + args.steps):
-            flush_w.zero_()
-            flush_r.max()
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             lay.build(idx, fused=fused)
@@ -296,234 +718,97 @@ def run_layout_only(args, local):
 
 
 def run_native(args, rank, world, local):
-    from counting_sort_bucketization_gb300 import binding
-
     init_dist(world, "nccl")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = wl.WORKLOADS[args.workload]
+    if args.tokens is not None:
+        w = w.replace(num_tokens=args.tokens)
     seed = wl.SEEDS[w.name] + 1000 * rank
-    inp = wl.make(w, seed)
-    N, K, H = w.num_tokens, w.topk, w.hidden
-    cap = wl.worst_case_rows(w)
-    stream = torch.cuda.current_stream(dev)
-
-    idx_d = inp["topk_idx"].to(dev)
-    x_d = inp["x"].to(dev)
-    sf_d = inp["sf"].to(dev) if inp["sf"] is not None else None
-    wt_d = inp["weights"].to(dev)
-    lay = binding.Layout(w, cap, device=dev)
-    recv = torch.empty((cap, H), dtype=x_d.dtype, device=dev)
-    recv_sf = torch.empty((cap, sf_d.shape[1]), dtype=sf_d.dtype, device=dev) if sf_d is not None else None
-    sf_cm = args.sf_col_major and sf_d is not None
-    # Column-major scale factors: the permute moves rows only, then its own kernel.
-    recv_sf_cm = binding.new_sf_col_major(sf_d.shape[1], cap, device=dev) if sf_cm else None
-    perm_sf, perm_recv_sf = (None, None) if sf_cm else (sf_d, recv_sf)
-    do_combine = w.row_dtype == "bf16"
-    out = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
-    # The combine's input: the round-trip stand-in expert applied once to a
-    # dispatched buffer (harness, untimed): rows of expert e scaled by 1 + e/384.
-    lay.build(idx_d)
-    lay.permute(x_d, recv, sf_d, recv_sf)
-    rows = int(lay.total_rows.item())
-    eo = torch.zeros((cap, H), dtype=torch.bfloat16, device=dev)
-    if do_combine:
-        off = lay.expert_offset.to(torch.int64)
-        row_e = torch.searchsorted(off[1:], torch.arange(rows, device=dev), right=True)
-        eo[:rows] = (recv[:rows].float() * inp["expert_scale"].to(dev)[row_e][:, None]).to(torch.bfloat16)
-    assert lay.error() == 0, "device error during set-up"
-    # Non-expand mode: one row per (token, rank reached), rank-contiguous, no padding.
-    ne = args.non_expand
-    if ne:
-        ne_cap = N * w.num_ranks
-        lay.rank_rows(idx_d, capacity_rows=ne_cap)
-        recv_ne = torch.empty((ne_cap, H), dtype=x_d.dtype, device=dev)
-        recv_ne_sf = torch.empty((ne_cap, sf_d.shape[1]), dtype=sf_d.dtype, device=dev) if sf_d is not None else None
-        lay.permute_ranks(x_d, recv_ne, sf_d, recv_ne_sf)
-        assert lay.error() == 0, "device error during set-up"
-    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-
-    def flush_l2():
-        flush_w.zero_()
-        flush_r.max()
-
-    # The step's kernels in order, one event after each (and one before the
-    # first): every timed interval holds exactly one step of the path.
-    stages = [("layout", lambda: lay.build(idx_d))]
-    if ne:
-        stages += [("rank_rows", lambda: lay.rank_rows(idx_d, capacity_rows=ne_cap)),
-                   ("permute_ranks", lambda: lay.permute_ranks(x_d, recv_ne, sf_d, recv_ne_sf))]
-    else:
-        stages.append(("permute", lambda: lay.permute(x_d, recv, perm_sf, perm_recv_sf)))
-        if sf_cm:
-            stages.append(("sf_col_major", lambda: lay.permute_sf_col_major(sf_d, recv_sf_cm)))
-        if do_combine:
-            stages.append(("combine", lambda: lay.combine(eo, wt_d, out)))
-
-    # The timed steps carry one event before and one after the whole step: an
-    # event between two kernels would stand between them in the stream and
-    # stop the next one from starting during the previous one's tail (the
-    # programmatic dependent launch the kernels are built for).  Per-kernel
-    # times come from a second loop with an event after every kernel.
-    def step(ev):
-        ev[0].record(stream)
-        for _, run in stages:
-            run()
-        ev[1].record(stream)
-
-    def step_per_kernel(ev):
-        ev[0].record(stream)
-        for i, (_, run) in enumerate(stages):
-            run()
-            ev[i + 1].record(stream)
-
-    new_events = lambda n: [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-    for _ in range(args.warmup):
-        flush_l2()
-        step(new_events(2))
-    torch.cuda.synchronize(dev)
-    assert lay.error() == 0, "device error during warm-up"
-
-    evs = [new_events(2) for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    launches0 = binding.kernel_launches()
-    sampler = ClockSampler(local) if (rank == 0 and not args.no_clocks) else None
-    if sampler:
-        sampler.__enter__()
-    t_wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush_l2()
-        step(evs[i])
-    torch.cuda.synchronize(dev)
-    t_wall = time.perf_counter() - t_wall0
-    barrier(world)
-    if sampler:
-        sampler.__exit__(None, None, None)
-    launches = binding.kernel_launches() - launches0
-    err = lay.error()
-    assert err == 0, f"device error {err} in the timed region"
-
-    step_ms = np.array([e[0].elapsed_time(e[1]) for e in evs])   # ms
-    ms_per_step = reduce_max(float(step_ms.mean()), world, dev)
-    # Per-kernel breakdown (untimed for the headline): the same steps with an event after each kernel.
-    n_break = min(args.steps, args.breakdown_steps)
-    kevs = [new_events(len(stages) + 1) for _ in range(n_break)]
-    for i in range(n_break):
-        flush_l2()
-        step_per_kernel(kevs[i])
-    torch.cuda.synchronize(dev)
-    per = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(len(stages))] for e in kevs])   # ms
-    kern_ms = dict(zip([name for name, _ in stages], per.mean(axis=0).tolist()))
-    ab = algorithmic_bytes(w, lay, sf_cm)
-    if ne:
-        # each routed token's row read once, one row written per (token, rank reached), the slots read
-        rows_ne = int(lay.rank_psum[-1].item())
-        rb_all = w.row_bytes + w.sf_row_bytes
-        ab["permute_ranks"] = ab["tokens_routed"] * rb_all + rows_ne * rb_all + N * w.topk * 4
-        ab["rows_non_expand"] = rows_ne
-    value = world * N / (ms_per_step / 1e3)
-    dispatch_ms = sum(v for k, v in kern_ms.items() if k != "combine")
-
-    # End to end through the public API with host buffers: pinned ids, rows
-    # and weights in, the combined tokens back (dispatch-only workloads: the
-    # receive rows back).  moe_dispatch_from_host and moe_combine_to_host
-    # overlap the copies with the kernels in chunks, and HostPipeline keeps
-    # `--e2e-lanes` batches in flight so one batch's copy back overlaps the
-    # next one's copy in.  Every copy is inside the timed region; each
-    # step's working set (rows, receive buffer) is larger than L2.
-    idx_h = inp["topk_idx"].pin_memory()
-    x_h = inp["x"].pin_memory()
-    sf_h = inp["sf"].pin_memory() if inp["sf"] is not None else None
-    wt_h = inp["weights"].pin_memory()
-    out_shape, out_dtype = ((N, H), torch.bfloat16) if do_combine else ((cap, H), x_d.dtype)
-    lanes = max(1, args.e2e_lanes)
-    outs_h = [torch.empty(out_shape, dtype=out_dtype).pin_memory() for _ in range(lanes)]
-    h2d = idx_h.numel() * 8 + x_h.numel() * x_h.element_size() + wt_h.numel() * 4 + \
-        (sf_h.numel() * 4 if sf_h is not None else 0)
-    d2h = outs_h[0].numel() * outs_h[0].element_size()
-    chunk_of = lambda n_chunks: -(-N // max(1, n_chunks))
+    profile = args.profile
+    sampler = ClockSampler(local).start() if (rank == 0 and not args.no_clocks and not profile) else None
+    peak = measured_peaks()
+    flush = Flusher(dev)
+    case = Case(w, seed, dev, non_expand=args.non_expand, sf_col_major=args.sf_col_major, eo_alias=profile,
+                keep_inputs=not profile)
+    t = time_case(case, args.steps, args.warmup, flush, world, sampler, args.breakdown_steps, args.enqueue_steps)
+    summ = case_summary(case, t, peak, world)
+    kern = t["kernels_ms"]
+    # The line's roofline: the HBM-bound kernel that takes the longest.
+    dom = max((s for s in HBM_STAGES if s in kern), key=lambda s: kern[s])
     e2e_line = None
-    e2e_steps = max(3, min(args.steps, args.e2e_steps))
-    expert = (lambda lay_, recv_, recv_sf_: eo) if do_combine else None
+    if not args.non_expand and not profile and not args.no_e2e:
+        e2e_line = run_e2e(case, args, world, dev)
+    line = {
+        "metric": METRIC, "value": summ["tokens_per_s"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.row_dtype == "bf16" else "fp8 rows (bytes moved)",
+        "data": "synthetic", "config": config_of(w),
+        "roofline": {**summ["rooflines"][dom],
+                     "note": "the HBM-bound kernel with the longest time; algorithmic bytes include the "
+                             "launch's last writes, still dirty in L2 when it ends (written back during the "
+                             "next kernel), so frac can read a little above 1 and traffic below the "
+                             "algorithmic bytes; frac_dram uses the measured DRAM bytes instead"},
+        "rooflines": summ["rooflines"],
+        "kernels_ms": kern, "kernels_gbs": summ["kernels_gbs"], "kernels_frac": summ["kernels_frac"],
+        "kernels_frac_dram": summ["kernels_frac_dram"],
+        "breakdown": {"steps": t["breakdown_steps"], "sum_of_kernels_ms": float(sum(kern.values())),
+                      "note": "kernels_ms come from separate steps with an event after every kernel; those "
+                              "events keep each kernel from starting during the previous one's tail, so their "
+                              "sum can exceed ms_per_step, which is timed per whole step"},
+        "dispatch_tokens_per_s": summ["dispatch_tokens_per_s"],
+        "layout": summ["layout"],
+        "host_enqueue_us_per_step": t["host_enqueue_us_per_step"],
+        "host_enqueue_note": f"wall time of {t['host_enqueue_steps']} steps' calls (Python binding + C ABI + "
+                            "launches) enqueued back to back, divided by the steps; no synchronisation inside",
+        "e2e": e2e_line,
+        "gpu_launches": t["launches"],
+        "wall_s_timed_region": t["wall_s"],
+        "step_ms_range": [t["step_ms_min"], t["step_ms_max"]],
+        "clocks": t["clocks"],
+    }
+    if args.non_expand:
+        line["config"]["layout_mode"] = "non-expand: one row per (token, rank reached), rank-contiguous, no padding"
+    if case.sf_d is not None:
+        line["config"]["sf_layout"] = ("column-major, ld = capacity rounded up to 4 words (e2e leg: row-major)"
+                                       if case.sf_cm else "row-major, moved by the permute")
+    if profile:
+        line["config"]["profile"] = "small footprint: no e2e leg, no CPU baseline, the combine reads the receive buffer"
+    inp_cpu = case.inp
+    del case
+    torch.cuda.empty_cache()
 
-    def e2e_ms_per_step(n_lanes, n_chunks):
-        pipe = binding.HostPipeline(w, cap, H, x_dtype=x_d.dtype, sf_cols=sf_d.shape[1] if sf_d is not None else 0,
-                                    lanes=n_lanes, chunk_tokens=chunk_of(n_chunks), device=dev)
-        for i in range(2 * n_lanes):
-            pipe.submit(idx_h, x_h, wt_h, outs_h[i % n_lanes], expert, sf_h)
-        pipe.join(stream)
-        torch.cuda.synchronize(dev)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for i in range(e2e_steps):
-            pipe.submit(idx_h, x_h, wt_h, outs_h[i % n_lanes], expert, sf_h)
-        pipe.join(stream)
-        b.record(stream)
-        torch.cuda.synchronize(dev)
-        assert pipe.errors() == [0] * n_lanes, "device error in the end-to-end steps"
-        return a.elapsed_time(b) / e2e_steps
-
-    if not ne:   # the end-to-end leg is the expand path's
-        e2e_step_ms = reduce_max(e2e_ms_per_step(lanes, args.e2e_chunks), world, dev)
-        # One batch in flight, its copies overlapped with the kernels in 4 chunks: the reference point.
-        e2e_one_ms = reduce_max(e2e_ms_per_step(1, 4), world, dev)
-        e2e_line = {"value": world * N / (e2e_step_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": e2e_steps, "chunks": args.e2e_chunks,
-                    "batches_in_flight": lanes,
-                    "value_one_batch_in_flight_4_chunks": world * N / (e2e_one_ms / 1e3),
-                    "api": "HostPipeline: moe_dispatch_from_host + moe_combine_to_host" if do_combine
-                    else "HostPipeline: moe_dispatch_from_host + receive rows copied back"}
+    # The other large workloads: a clocked loop of their own each.
+    if world == 1 and not profile and not args.no_per_config:
+        per = {}
+        only = set(args.per_config_only.split(",")) if args.per_config_only else None
+        for key, name, opts in PER_CONFIG:
+            if (key == line["config"]["workload"] and not opts) or (only is not None and key not in only):
+                continue
+            cw = wl.WORKLOADS[name]
+            c = Case(cw, wl.SEEDS[name], dev, **opts)
+            steps = max(args.steps, args.per_config_steps)
+            ct = time_case(c, steps, max(3, args.warmup), flush, world, sampler, args.breakdown_steps,
+                           args.enqueue_steps)
+            s = case_summary(c, ct, peak, world)
+            s["steps"], s["warmup"] = steps, max(3, args.warmup)
+            s["config"] = {"workload": name, **{k: v for k, v in config_of(cw).items() if k != "l2"},
+                           **({"layout_mode": "non-expand"} if opts.get("non_expand") else {}),
+                           **({"sf_layout": "column-major"} if opts.get("sf_col_major") else {})}
+            per[key] = s
+            del c
+            torch.cuda.empty_cache()
+        line["per_config"] = per
+    if sampler is not None:
+        sampler.stop()
 
     if rank != 0:
         return
-    peaks = measured_peaks()
-    dom = "permute_ranks" if ne else "permute"
-    permute_s = kern_ms[dom] / 1e3
-    achieved = ab[dom] / permute_s / 1e9
-    traffic = None
-    if PERMUTE_TRAFFIC.get("sha256") == sources_sha256(PERMUTE_SOURCES):
-        traffic = PERMUTE_TRAFFIC["bytes_per_launch"].get(w.name + ("/non-expand" if ne else ""))
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(w),
-        "roofline": {"kernel": "permute_dyn_kernel", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                     "peak_source": peaks["source"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": traffic, "algorithmic_bytes_per_launch": ab[dom],
-                     "note": "algorithmic bytes include the launch's last writes, still dirty in L2 when it "
-                             "ends (written back during the next kernel): frac can read a little above 1 and "
-                             "traffic below the algorithmic bytes"},
-        "kernels_ms": dict(kern_ms) if ne else {
-            "layout": kern_ms["layout"], "permute": kern_ms["permute"],
-            "sf_col_major": kern_ms.get("sf_col_major"), "combine": kern_ms.get("combine")},
-        "kernels_gbs": {"permute_ranks": achieved} if ne else {
-            "permute": ab["permute"] / permute_s / 1e9,
-            "sf_col_major": (ab["sf_col_major"] / (kern_ms["sf_col_major"] / 1e3) / 1e9) if sf_cm else None,
-            "combine": (ab["combine"] / (kern_ms["combine"] / 1e3) / 1e9) if do_combine else None},
-        "breakdown": {"steps": n_break, "sum_of_kernels_ms": float(sum(kern_ms.values())),
-                      "note": "kernels_ms come from separate steps with an event after every kernel; those "
-                              "events keep each kernel from starting during the previous one's tail, so their "
-                              "sum exceeds ms_per_step, which is timed per whole step"},
-        "dispatch_tokens_per_s": world * N / (dispatch_ms / 1e3),
-        "layout": {"valid_pairs": ab["P"], "rows": ab["rows"], "tokens_routed": ab["tokens_routed"]},
-        "e2e": e2e_line,
-        "gpu_launches": launches,
-        "wall_s_timed_region": t_wall,
-        "clocks": sampler.summary() if sampler else None,
-    }
-    if ne:
-        line["config"]["layout_mode"] = "non-expand: one row per (token, rank reached), rank-contiguous, no padding"
-        line["layout"]["rows_non_expand"] = ab["rows_non_expand"]
-    if sf_d is not None:
-        line["config"]["sf_layout"] = ("column-major, ld = capacity rounded up to 4 words (e2e leg: row-major)"
-                                       if sf_cm else "row-major, moved by the permute")
-    if world == 1 and not args.no_cpu_baseline and not ne:
-        runner = OracleRunner(w, inp)
+    if world == 1 and not args.no_cpu_baseline and not args.non_expand and not profile:
+        runner = OracleRunner(w, inp_cpu)
         tps, passes = runner.time_passes(args.cpu_seconds, args.cpu_max_passes)
         line["cpu_baseline"] = {"value": tps, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                "sample": f"{passes} full pass(es) of the {w.name} workload ({N} tokens): "
+                                "sample": f"{passes} full pass(es) of the {w.name} workload ({w.num_tokens} tokens): "
                                           f"layout, permute with zero padding, combine; single-threaded C",
                                 **host_info()}
     print(json.dumps(line), flush=True)
@@ -573,26 +858,37 @@ def run_reference(args, rank, world):
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", choices=list(wl.WORKLOADS), default="decode")
+    ap.add_argument("--workload", choices=list(wl.WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="tokens per batch instead of the workload's (same recipe); for small profiling cases")
     ap.add_argument("--e2e-steps", type=int, default=200,
                     help="timed end-to-end steps (enough that filling and draining the batches in flight is ~1 %%)")
     ap.add_argument("--e2e-chunks", type=int, default=1, help="token chunks the host copies are split into")
     ap.add_argument("--e2e-lanes", type=int, default=3, help="batches in flight in the end-to-end leg")
+    ap.add_argument("--no-e2e", action="store_true", help="leave out the end-to-end leg")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-max-passes", type=int, default=20)
-    ap.add_argument("--ref-seconds", type=float, default=90.0)
+    ap.add_argument("--ref-seconds", type=float, default=75.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="leave out the other workloads' clocked loops")
+    ap.add_argument("--per-config-only", default=None,
+                    help="comma-separated keys of the other workloads' loops to run (default: all of "
+                         + ", ".join(k for k, _, _ in PER_CONFIG) + ")")
+    ap.add_argument("--per-config-steps", type=int, default=300,
+                    help="timed steps of each other workload's loop (at least --steps)")
+    ap.add_argument("--profile", action="store_true",
+                    help="small device footprint for ncu: no end-to-end leg, no CPU baseline, no other "
+                         "workloads, no clock sampling; the combine reads the receive buffer")
     ap.add_argument("--sf-col-major", action="store_true",
                     help="fp8 workloads: scale factors column-major (TMA-aligned) by their own kernel")
     ap.add_argument("--ids-int32", action="store_true", help="--layout-only: int32 routing ids")
-    ap.add_argument("--tokens", type=int, default=None,
-                    help="--layout-only: tokens per batch instead of the workload's (same routing recipe)")
     ap.add_argument("--breakdown-steps", type=int, default=300,
                     help="steps of the per-kernel breakdown loop (after the timed steps)")
+    ap.add_argument("--enqueue-steps", type=int, default=50, help="steps of the host enqueue-time loop")
     ap.add_argument("--non-expand", action="store_true",
                     help="time the non-expand layout instead: layout, rank rows, rank-contiguous permute")
     ap.add_argument("--layout-only", action="store_true",

@@ -1,6 +1,7 @@
 """bench.py's native JSON line on a GB300: one line, with every key the
 benchmark contract asks for and the types it asks for (a short run of the
-decode workload: 5 timed steps after 3 warm-up steps)."""
+decode workload: 5 timed steps after 3 warm-up steps, one other workload's
+clocked loop)."""
 import json
 import os
 import subprocess
@@ -18,9 +19,10 @@ def _number(v):
 
 
 def test_native_line_keeps_the_contract():
-    proc = subprocess.run([sys.executable, os.path.join(REPO, "bench.py"), "--steps", "5", "--warmup", "3",
-                           "--e2e-steps", "5", "--breakdown-steps", "5", "--cpu-seconds", "1",
-                           "--cpu-max-passes", "1"],
+    proc = subprocess.run([sys.executable, os.path.join(REPO, "bench.py"), "--workload", "decode", "--steps", "5",
+                           "--warmup", "3", "--e2e-steps", "5", "--breakdown-steps", "5", "--cpu-seconds", "1",
+                           "--cpu-max-passes", "1", "--per-config-only", "decode/non-expand",
+                           "--per-config-steps", "20"],
                           cwd=REPO, capture_output=True, text=True, timeout=600)
     assert proc.returncode == 0, proc.stderr[-3000:]
     lines = [ln for ln in proc.stdout.splitlines() if ln.strip()]
@@ -41,5 +43,17 @@ def test_native_line_keeps_the_contract():
     assert e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert isinstance(d["gpu_launches"], int) and d["gpu_launches"] >= 5 * 3
     assert "clocks" in d
+    assert e2e["link_ceiling_tokens_per_s"] > 0 and 0 < e2e["frac_of_link"]
+    assert _number(d["host_enqueue_us_per_step"]) and d["host_enqueue_us_per_step"] > 0
+    assert set(d["rooflines"]) == {"permute", "combine"}
+    for r in d["rooflines"].values():
+        assert r["bound"] == "hbm" and abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
+    clk = d["clocks"]
+    assert clk is not None and clk["samples"] >= 1 and _number(clk["sm_mhz"]) and isinstance(clk["reasons"], list)
+    pc = d["per_config"]
+    assert list(pc) == ["decode/non-expand"]
+    ne = pc["decode/non-expand"]
+    assert ne["steps"] == 20 and ne["config"]["layout_mode"] == "non-expand"
+    assert "permute_ranks" in ne["kernels_ms"] and ne["clocks"] is not None
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["unit"] == "tokens/s" and _number(cb["value"])
