@@ -60,7 +60,7 @@ inline TilePlan make_tile_plan(int64_t N, int K) {
 struct WorkspaceLayout {
   size_t err_off = 0;
   size_t bar_off = 16;   // two unsigned: grid-barrier arrival counter (zero between launches), spare
-  size_t work_off = 32;  // two unsigned: permute's token counter, finished CTAs
+  size_t work_off = 32;  // four unsigned: permute's unit counter, its finished CTAs; the combine's two
   size_t hist_off = 256;
   size_t rhist_off = 0;
   size_t bytes = 0;

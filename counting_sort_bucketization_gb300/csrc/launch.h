@@ -78,6 +78,8 @@ struct CombineArgs {
   int64_t num_tokens;
   int topk;
   int* err;
+  unsigned* work;              // [2] token counter + finished-CTA counter (zero between launches)
+  uint64_t wait_ns;            // bound on each mbarrier wait (set by launch_combine)
 };
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t stream);

@@ -408,6 +408,7 @@ int moe_combine_unpermute(const moe_layout_desc* desc, const void* expert_out, i
   a.num_tokens = desc->num_tokens;
   a.topk = desc->topk;
   a.err = at<int>(workspace, w.err_off);
+  a.work = at<unsigned>(workspace, w.work_off) + 2;
   return cuda_status(launch_combine(a, static_cast<cudaStream_t>(stream)));
 }
 
