@@ -4,10 +4,12 @@
 // Method: page "07 DeepEP Counting Sort / Bucketization", [CS] below.
 //   count   [CS] §4.2: per-expert counts and per-rank counts with one count
 //           per token per rank.  As on the page, each CTA first counts in a
-//           shared-memory histogram and warps deduplicate ranks with
-//           __match_any_sync; unlike the page, the per-CTA histograms are
-//           kept (one column per tile) instead of being reduced into one
-//           global array, because the stable scatter needs every tile's base.
+//           shared-memory histogram; the rank deduplication the page does
+//           with a warp match is done here from the token's own ids in shared
+//           memory (a token counts in a rank on its first pair there).  Unlike
+//           the page, the per-CTA histograms are kept (one column per tile)
+//           instead of being reduced into one global array, because the
+//           stable scatter needs every tile's base.
 //   scan    [CS] §5.2-§5.5, §7.2: the page scans on one SM after a grid-wide
 //           reduction; here one warp per expert scans that expert's tile
 //           column, and every rank CTA recomputes the (small) aligned
@@ -15,9 +17,10 @@
 //   rank    [CS] §6.4 assigns slots with atomicAdd on the exclusive sum,
 //           which makes the order inside a segment depend on scheduling.
 //           Here the slot is expert_offset[e] + (pairs of e in earlier
-//           tiles) + (pairs of e earlier in this tile), the last term from
-//           __match_any_sync + popc within a warp and a per-expert scan over
-//           the warps: token-ascending and deterministic.
+//           tiles) + (pairs of e earlier in this tile), the last term from a
+//           per-warp running count per expert, advanced one token at a time
+//           (a token's pairs name distinct experts), and a per-expert scan
+//           over the warps: token-ascending and deterministic.
 //
 // Two ways to run the three phases:
 //   - three kernels (count_tiles, scan_columns, rank_maps), chained with
@@ -47,7 +50,10 @@ constexpr unsigned kFull = 0xffffffffu;
 // id >= E -> -1 and flagged.
 // Each thread issues kStageBatch independent loads before it uses any, so a
 // tile of thousands of pairs costs a few memory latencies, not one per pair.
-constexpr int kStageBatch = 8;
+#ifndef MOE_LAYOUT_STAGE_BATCH
+#define MOE_LAYOUT_STAGE_BATCH 8
+#endif
+constexpr int kStageBatch = MOE_LAYOUT_STAGE_BATCH;
 
 template <typename IdT>
 __device__ __forceinline__ void stage_tile_ids(const IdT* __restrict__ topk_idx,
@@ -113,6 +119,57 @@ __device__ __forceinline__ TileCoords tile_coords(const TilePlan& plan, int64_t 
   return c;
 }
 
+// What pair (t, k) with expert e learns from token t's own ids (contiguous
+// in the staged tile, `tok` points at the first): how many of the token's
+// earlier and later pairs name e too (duplicates: the method's precondition
+// excludes them, the pair-by-pair definition still orders them by k), and
+// whether an earlier or a later pair of the token reaches e's rank (the
+// token's last pair reaching a rank carries the non-expand row).
+struct TokenView {
+  int dup_before, dup_after;
+  bool first_in_rank, last_in_rank;
+};
+
+__device__ __forceinline__ TokenView token_view(const int* tok, int K, int k, int e, int L) {
+  TokenView v{0, 0, true, true};
+  const int r_lo = (e / L) * L;
+  for (int j = 0; j < K; ++j) {
+    const int f = tok[j];
+    if (j == k || f < 0) continue;
+    if (f == e) {
+      if (j < k) ++v.dup_before; else ++v.dup_after;
+    }
+    if (f >= r_lo && f < r_lo + L) {
+      if (j < k) v.first_in_rank = false; else v.last_in_rank = false;
+    }
+  }
+  return v;
+}
+
+// Whether this pair is the one that counts its token in rank r ([CS] §4.2:
+// a token counts once in each rank it reaches).  Warp-collective: every lane
+// calls it, `valid` false for lanes without a pair.  Up to 32 ranks, each
+// token of the chunk gets a word of rank bits in shared memory and the pair
+// whose atomicOr sets the bit counts; beyond that, a warp match on
+// (token, rank).  Measured on GB300 (one-call layout of 131072 x 8 ids): the
+// bit words took the rank pass from 15.4 to 10.7 us.
+__device__ __forceinline__ bool counts_token_in_rank(bool valid, int tic, int r, int tpc, int R) {
+  const int warp = threadIdx.x / kWarpSize, lane = threadIdx.x % kWarpSize;
+  if (R <= kWarpSize) {
+    __shared__ unsigned tok_ranks_s[kLayoutWarps][kWarpSize];
+    unsigned* words = tok_ranks_s[warp];
+    if (lane < tpc) words[lane] = 0u;
+    __syncwarp();
+    bool first = false;
+    if (valid) first = (atomicOr(&words[tic], 1u << r) & (1u << r)) == 0u;
+    __syncwarp();
+    return first;
+  }
+  const unsigned key = valid ? static_cast<unsigned>(tic * MOE_MAX_EXPERTS + r) : (0x80000000u | lane);
+  const unsigned peers = __match_any_sync(kFull, key);
+  return valid && __ffs(peers) - 1 == lane;
+}
+
 // ------------------------------------------------------- phase: count
 // ids_s holds the tile's staged ids; hist_s [E] and rhist_s [R] are zeroed.
 // Writes the tile's column of hist [E][T] and rhist [R][T].
@@ -128,17 +185,9 @@ __device__ void count_phase(const TilePlan& plan, int K, int E, int R, int tile,
     const bool in = lane < plan.lanes && tok < ntok;
     const int e = in ? ids_s[chunk * plan.lanes + lane] : -1;
     const bool valid = e >= 0;
-    // Experts: one shared atomic per distinct expert in the chunk.
-    const unsigned peers = __match_any_sync(kFull, valid ? static_cast<unsigned>(e)
-                                                         : (0x80000000u | lane));
-    if (valid && __ffs(peers) - 1 == lane) atomicAdd(&hist_s[e], __popc(peers));
-    // Ranks: lanes of the same token that hit the same rank form one group;
-    // only its lowest lane counts ([CS] §4.2 deduplication).
     const int r = valid ? e / L : 0;
-    const unsigned rkey = valid ? static_cast<unsigned>(tok_in_chunk * MOE_MAX_EXPERTS + r)
-                                : (0x80000000u | lane);
-    const unsigned rpeers = __match_any_sync(kFull, rkey);
-    if (valid && __ffs(rpeers) - 1 == lane) atomicAdd(&rhist_s[r], 1);
+    if (valid) atomicAdd(&hist_s[e], 1);
+    if (counts_token_in_rank(valid, tok_in_chunk, r, plan.tpc, R)) atomicAdd(&rhist_s[r], 1);
   }
   __syncthreads();
   const int64_t T = plan.tiles;
@@ -207,11 +256,22 @@ struct RankArgs {
 };
 
 // Rank of each pair among the same expert's pairs earlier in its warp's run
-// (lr_s), and each warp's per-expert counts (cnt_s[warp][e], zeroed before).
-// When rhist_s is given, also the tile's rank counts, once per token and
-// rank ([CS] §4.2 deduplication): the fused kernel needs no separate count pass.
+// (lr_s), each warp's per-expert counts (cnt_s[warp][e], zeroed before) and
+// the tile's per-expert counts (ecount_s, zeroed before).  When rhist_s is
+// given, also the tile's rank counts, once per token and rank ([CS] §4.2
+// deduplication): the fused kernel needs no separate count pass.
+//
+// The chunk's tokens are ranked one at a time: a token's pairs name distinct
+// experts, so each reads its expert's running count and writes it back one
+// higher, and pairs end up ranked in (t, k) order.  Measured on GB300 this
+// beat a warp match per chunk (one-call layout of 131072 x 8 ids: rank pass
+// 15.4 -> 10.7 us with the rank bits of counts_token_in_rank).  A token that
+// names one expert twice (outside the method's precondition, but still
+// defined pair by pair) would lose a count; the per-warp sums are checked
+// against the tile's exact counts, and a tile that fails is ranked again with
+// warp matches, which order repeated pairs by k.
 __device__ void rank_pass(const TilePlan& plan, int K, int E, int R, int ntok, const int* ids_s, int* cnt_s,
-                          int* lr_s, int* rhist_s) {
+                          int* lr_s, int* ecount_s, int* rhist_s) {
   const int warp = threadIdx.x / kWarpSize, lane = threadIdx.x % kWarpSize;
   const int L = E / R;
   const int tok_in_chunk = lane / K;
@@ -223,8 +283,41 @@ __device__ void rank_pass(const TilePlan& plan, int K, int E, int R, int ntok, c
     const int pair = chunk * plan.lanes + lane;
     const int e = in ? ids_s[pair] : -1;
     const bool valid = e >= 0;
-    const unsigned peers = __match_any_sync(kFull, valid ? static_cast<unsigned>(e)
-                                                         : (0x80000000u | lane));
+    for (int i = 0; i < plan.tpc; ++i) {
+      const bool mine = valid && tok_in_chunk == i;
+      const int base = mine ? my_cnt[e] : 0;
+      __syncwarp();
+      if (mine) {
+        my_cnt[e] = base + 1;
+        lr_s[pair] = base;
+      }
+      __syncwarp();
+    }
+    if (valid) atomicAdd(&ecount_s[e], 1);
+    if (rhist_s != nullptr) {
+      const int r = valid ? e / L : 0;
+      if (counts_token_in_rank(valid, tok_in_chunk, r, plan.tpc, R)) atomicAdd(&rhist_s[r], 1);
+    }
+  }
+  __syncthreads();
+  bool lost = false;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int sum = 0;
+    for (int w = 0; w < kLayoutWarps; ++w) sum += cnt_s[w * E + e];
+    lost |= sum != ecount_s[e];
+  }
+  if (!__syncthreads_or(lost)) return;
+  // A repeated expert inside a token: rank the tile again, repeats in k order.
+  for (int i = threadIdx.x; i < kLayoutWarps * E; i += blockDim.x) cnt_s[i] = 0;
+  __syncthreads();
+  for (int c = 0; c < plan.cpw; ++c) {
+    const int chunk = warp * plan.cpw + c;
+    const int tok = chunk * plan.tpc + tok_in_chunk;
+    const bool in = lane < plan.lanes && tok < ntok;
+    const int pair = chunk * plan.lanes + lane;
+    const int e = in ? ids_s[pair] : -1;
+    const bool valid = e >= 0;
+    const unsigned peers = __match_any_sync(kFull, valid ? static_cast<unsigned>(e) : (0x80000000u | lane));
     const int base = valid ? my_cnt[e] : 0;
     __syncwarp();
     if (valid) {
@@ -232,13 +325,6 @@ __device__ void rank_pass(const TilePlan& plan, int K, int E, int R, int ntok, c
       lr_s[pair] = base + __popc(peers & ptx::lanemask_lt());
     }
     __syncwarp();
-    if (rhist_s != nullptr) {
-      const int r = valid ? e / L : 0;
-      const unsigned rkey = valid ? static_cast<unsigned>(tok_in_chunk * MOE_MAX_EXPERTS + r)
-                                  : (0x80000000u | lane);
-      const unsigned rpeers = __match_any_sync(kFull, rkey);
-      if (valid && __ffs(rpeers) - 1 == lane) atomicAdd(&rhist_s[r], 1);
-    }
   }
   __syncthreads();
 }
@@ -388,12 +474,14 @@ __global__ void __launch_bounds__(kLayoutThreads)
   int* cnt_s = gap_s + a.E;                     // [kLayoutWarps][E]
   int* ids_s = cnt_s + kLayoutWarps * a.E;      // [tile pairs]
   int* lr_s = ids_s + plan.tile_tokens * a.K;   // [tile pairs]
+  int* ecount_s = lr_s + plan.tile_tokens * a.K;   // [E]
   __shared__ int warp_tot_s[kLayoutWarps];
   const TileCoords tc = tile_coords(plan, a.N, blockIdx.x);
   for (int i = threadIdx.x; i < kLayoutWarps * a.E; i += blockDim.x) cnt_s[i] = 0;
+  for (int i = threadIdx.x; i < a.E; i += blockDim.x) ecount_s[i] = 0;
   stage_tile_ids(topk_idx, tc.t0 * a.K, tc.ntok * a.K, a.E, ids_s, a.err);
   __syncthreads();   // staged ids and zeroed counters visible to every warp
-  rank_pass(plan, a.K, a.E, a.R, tc.ntok, ids_s, cnt_s, lr_s, nullptr);
+  rank_pass(plan, a.K, a.E, a.R, tc.ntok, ids_s, cnt_s, lr_s, ecount_s, nullptr);
   ptx::grid_dependency_wait();
   ptx::grid_dependency_launch_dependents();
   rank_finish(plan, a, blockIdx.x, tc, ids_s, off_s, gap_s, cnt_s, lr_s, warp_tot_s);
@@ -444,6 +532,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
   int* off_s = cnt_s + kLayoutWarps * E;        // [E+1]
   int* gap_s = off_s + (E + 1);                 // [E]
   int* rhist_s = gap_s + E;                     // [R]
+  int* ecount_s = rhist_s + R;                  // [E]
   __shared__ int warp_tot_s[kLayoutWarps];
   __shared__ int flag_s;
   const int tile = blockIdx.x;
@@ -451,19 +540,15 @@ __global__ void __launch_bounds__(kLayoutThreads)
   const TileCoords tc = tile_coords(plan, a.N, tile);
   for (int i = threadIdx.x; i < kLayoutWarps * E; i += blockDim.x) cnt_s[i] = 0;
   for (int i = threadIdx.x; i < R; i += blockDim.x) rhist_s[i] = 0;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) ecount_s[i] = 0;
   ptx::grid_dependency_wait();
   ptx::grid_dependency_launch_dependents();
   stage_tile_ids(topk_idx, tc.t0 * K, tc.ntok * K, E, ids_s, a.err);
   __syncthreads();
   // One pass over the tile's pairs: ranks inside each warp's run, per-warp
-  // expert counts, deduplicated rank counts.  The tile's expert count is the
-  // sum of the per-warp counts.
-  rank_pass(plan, K, E, R, tc.ntok, ids_s, cnt_s, lr_s, rhist_s);
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int c = 0;
-    for (int w = 0; w < kLayoutWarps; ++w) c += cnt_s[w * E + e];
-    hist[static_cast<int64_t>(e) * T + tile] = c;
-  }
+  // and per-tile expert counts, deduplicated rank counts.
+  rank_pass(plan, K, E, R, tc.ntok, ids_s, cnt_s, lr_s, ecount_s, rhist_s);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[static_cast<int64_t>(e) * T + tile] = ecount_s[e];
   for (int r = threadIdx.x; r < R; r += blockDim.x) rhist[static_cast<int64_t>(r) * T + tile] = rhist_s[r];
   if (!grid_barrier(bar, gridDim.x + a.barrier_extra, a.err, &flag_s, a.wait_ns)) return;
   scan_phase(hist, rhist, plan.tiles, E, R, expert_count, rank_count);
@@ -476,11 +561,11 @@ __global__ void __launch_bounds__(kLayoutThreads)
 // [CS] §6.2 (Scatter 1): one row per (token, rank) the token reaches, in
 // rank r's block [start_r, start_r + rank_count[r]) where start_r is the
 // exclusive sum of rank_count; tokens ascending inside a block.  The row goes
-// to the token's highest k reaching r (the master lane: the highest lane of
-// the __match_any_sync group of that token and rank); the other slots get -1.
-// The slot is start_r + (rows of r in earlier tiles, from the scanned rank
-// histogram) + (rows of r earlier in this tile: match_any + popc among the
-// master lanes, a per-warp running count, a scan over the warps).
+// to the token's highest k reaching r (the master lane of that token and
+// rank); the other slots get -1.  The slot is start_r + (rows of r in earlier
+// tiles, from the scanned rank histogram) + (rows of r earlier in this tile:
+// a per-warp running count per rank advanced one token at a time, and a scan
+// over the warps).
 struct RankRowsArgs {
   int64_t N;
   int K, E, R;
@@ -511,7 +596,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
   // tile and rank each token's master lanes inside its warp.
   stage_tile_ids(topk_idx, tc.t0 * K, tc.ntok * K, E, ids_s, a.err);
   __syncthreads();
-  const int tok_in_chunk = lane / K;
+  const int tok_in_chunk = lane / K, k = lane % K;
   int* my_cnt = cnt_s + warp * R;
   for (int c = 0; c < plan.cpw; ++c) {
     const int chunk = warp * plan.cpw + c;
@@ -521,17 +606,21 @@ __global__ void __launch_bounds__(kLayoutThreads)
     const int e = in ? ids_s[pair] : -1;
     const bool valid = e >= 0;
     const int r = valid ? e / L : 0;
-    // Lanes of one token reaching one rank; the highest of them is the master.
-    const unsigned grp = __match_any_sync(kFull, valid ? static_cast<unsigned>(tok_in_chunk * MOE_MAX_EXPERTS + r)
-                                                       : (0x80000000u | lane));
-    const bool master = valid && (31 - __clz(grp)) == lane;
-    // Masters of the same rank, in lane (= token) order.
-    const unsigned peers = __match_any_sync(kFull, master ? static_cast<unsigned>(r) : (0x80000000u | lane));
-    const int base = master ? my_cnt[r] : 0;
-    __syncwarp();
-    if (master && __ffs(peers) - 1 == lane) my_cnt[r] = base + __popc(peers);
-    if (in) lr_s[pair] = master ? base + __popc(peers & ptx::lanemask_lt()) : -1;
-    __syncwarp();
+    // The master is the token's last pair reaching r.
+    const bool master = valid && token_view(ids_s + pair - k, K, k, e, L).last_in_rank;
+    // Masters ranked per rank in token order, the chunk's tokens one at a
+    // time (a token's masters reach distinct ranks).
+    for (int i = 0; i < plan.tpc; ++i) {
+      const bool mine = master && tok_in_chunk == i;
+      const int base = mine ? my_cnt[r] : 0;
+      __syncwarp();
+      if (mine) {
+        my_cnt[r] = base + 1;
+        lr_s[pair] = base;
+      }
+      __syncwarp();
+    }
+    if (in && !master) lr_s[pair] = -1;
   }
   ptx::grid_dependency_wait();
   ptx::grid_dependency_launch_dependents();
@@ -604,7 +693,7 @@ __global__ void __launch_bounds__(kLayoutThreads)
 size_t fused_smem_bytes(const moe_layout_desc& d, const TilePlan& p) {
   const size_t pairs = static_cast<size_t>(p.tile_tokens) * d.topk;
   const size_t E = d.num_experts;
-  return sizeof(int) * (2 * pairs + kLayoutWarps * E + 2 * E + 1 + d.num_ranks);
+  return sizeof(int) * (2 * pairs + kLayoutWarps * E + 3 * E + 1 + d.num_ranks);
 }
 
 // Whether every tile's CTA of the fused kernel can be resident at once
@@ -649,7 +738,7 @@ size_t count_smem_bytes(const moe_layout_desc& d, const TilePlan& p) {
 }
 
 size_t rank_smem_bytes(const moe_layout_desc& d, const TilePlan& p) {
-  return sizeof(int) * (2 * static_cast<size_t>(d.num_experts) + 1 +
+  return sizeof(int) * (3 * static_cast<size_t>(d.num_experts) + 1 +
                         static_cast<size_t>(kLayoutWarps) * d.num_experts +
                         2 * static_cast<size_t>(p.tile_tokens) * d.topk);
 }
