@@ -25,11 +25,12 @@
 // Two ways to run the three phases:
 //   - three kernels (count_tiles, scan_columns, rank_maps), chained with
 //     programmatic dependent launch: the two-call API, and the one-call build
-//     while a tile holds one chunk per warp (batches up to ~64 k pairs) or when
-//     the tiles do not all fit on the GPU at once.  The rank kernel stages and
-//     ranks its ids before its wait, overlapping the column scan;
+//     until a tile holds the most chunks per warp (batches up to ~1 M pairs at
+//     top-8) or when the tiles do not all fit on the GPU at once.  The rank
+//     kernel stages and ranks its ids before its wait, overlapping the count
+//     and the column scan;
 //   - one cooperative kernel (layout_fused_kernel) with two grid barriers,
-//     the one-call build from two chunks per warp when every tile's CTA fits
+//     the one-call build at the largest tile plan when every tile's CTA fits
 //     on the GPU at once.  The tile's ids stay in shared memory from the count
 //     to the rank phase, and two launches and their gaps disappear.  Its
 //     barrier waits are bounded (MOE_ERR_TIMEOUT).
@@ -807,11 +808,14 @@ cudaError_t launch_build_t(const moe_layout_desc& d, const TilePlan& p, const Id
                            int32_t* rank_count, int32_t* hist, int32_t* rhist, unsigned* barrier_words,
                            const RankArgs& a, cudaStream_t stream) {
   const size_t smem = fused_smem_bytes(d, p);
-  // With one chunk per warp (up to ~64k pairs) the three PDL-chained kernels
-  // measured faster on GB300 than the cooperative kernel's two grid barriers
-  // (decode: 13.7 vs 14.5 us); from two chunks per warp on, the fused kernel
-  // wins (32768 x 8 ids: 19.6 vs 21.3 us; 131072 x 8: 37.1 vs 50.4 us).
-  if (p.cpw < 2 || !fused_fits<IdT>(p, smem)) {
+  // The three PDL-chained kernels rank each tile before the rank kernel's
+  // wait, overlapping the count and the column scan; the cooperative kernel
+  // does the phases one after another but saves two launches.  Measured on
+  // GB300 (one-call layout, top-8; chained / cooperative): 16384 tokens 13.8 /
+  // 16.5 us, 65536 21.8 / 22.1, 98304 25.7 / 26.6, 131072 (16 chunks per
+  // warp) 31.2 / 30.4.  So the cooperative kernel runs only when a tile holds
+  // the most chunks per warp and every tile's CTA fits on the GPU at once.
+  if (p.cpw < kMaxChunksPerWarp || !fused_fits<IdT>(p, smem)) {
     cudaError_t st = launch_count_t(d, p, topk_idx, expert_count, rank_count, a.err, hist, rhist, stream);
     if (st != cudaSuccess) return st;
     return launch_rank_t(d, p, topk_idx, a, stream);

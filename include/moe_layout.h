@@ -139,11 +139,12 @@ MOE_API int moe_layout_scan(const moe_layout_desc* desc, const int64_t* topk_idx
 
 /*
  * moe_layout_count followed by moe_layout_scan, in one call, with the same
- * arguments and results.  When every tile of the problem fits on the GPU at
- * once it runs as a single cooperative kernel (count, per-expert scan over
- * tiles, rank) with two grid-wide barriers whose waits are bounded
- * (MOE_ERR_TIMEOUT, after which the workspace must be zero-filled again);
- * otherwise it runs the two calls' kernels.
+ * arguments and results.  For the largest batches (about a million pairs and
+ * up), when every tile of the problem fits on the GPU at once, it runs as a
+ * single cooperative kernel (count, per-expert scan over tiles, rank) with
+ * two grid-wide barriers whose waits are bounded (MOE_ERR_TIMEOUT, after
+ * which the workspace must be zero-filled again); otherwise it runs the two
+ * calls' kernels.
  */
 MOE_API int moe_layout_build(const moe_layout_desc* desc, const int64_t* topk_idx,
                              int32_t* expert_count, int32_t* rank_count,

@@ -212,8 +212,10 @@ EDGE = [
     _w(500, 4, 16, 4, 4096, H=16),               # alignment 4096: nearly every receive row is padding
     _w(1500, 8, 64, 8, 4, H=7168, row_dtype="fp8"),  # rows cut in 2 pieces, scale rows with the first
     _w(3000, 8, 64, 8, 16, H=5000),              # rows cut in 3 pieces, the last one shorter
-    _w(40007, 3, 40, 5, 16, H=16),               # one-call layout in the cooperative kernel, ragged last tile
+    _w(40007, 3, 40, 5, 16, H=16),               # two chunks per warp, ragged last tile
     _w(70001, 1, 64, 8, 4, H=16),                # the same with K = 1
+    _w(330001, 3, 40, 5, 16, H=16),              # one-call layout in the cooperative kernel, ragged last tile
+    _w(1000001, 1, 64, 8, 4, H=16),              # the same with K = 1
 ]
 
 
@@ -377,19 +379,22 @@ def test_kernel_launch_counter_moves():
     before = binding.kernel_launches()
     full_case(wl.WORKLOADS["tiny"], 0, fused=False)
     assert binding.kernel_launches() - before == 5     # count, column scan, rank, permute, combine
-    # One-call build: the same three chained kernels while a tile holds one chunk per warp ...
+    # One-call build: the same three chained kernels until a tile holds 16 chunks per warp ...
     before = binding.kernel_launches()
     full_case(wl.WORKLOADS["tiny"], 0, fused=True)
     assert binding.kernel_launches() - before == 5
-    # ... and the cooperative kernel from two chunks per warp on
     before = binding.kernel_launches()
     full_case(_w(40007, 3, 40, 5, 16, H=16), 1, fused=True)
+    assert binding.kernel_launches() - before == 5
+    # ... and then the cooperative kernel
+    before = binding.kernel_launches()
+    full_case(_w(330001, 3, 40, 5, 16, H=16), 1, fused=True)
     assert binding.kernel_launches() - before == 3     # fused layout, permute, combine
 
 
 @pytest.mark.parametrize("w", [
     _w(4096, 8, 256, 8, 128, H=64),      # the chained layout kernels
-    _w(20000, 8, 256, 8, 128, H=64),     # the cooperative layout kernel
+    _w(131072, 8, 256, 8, 128, H=64),    # the cooperative layout kernel
 ], ids=["chained", "cooperative"])
 def test_back_to_back_on_one_workspace(w):
     """Three different routings through one workspace with no host synchronisation

@@ -38,8 +38,8 @@ def u8(t):
 
 
 def test_grid_barrier_runs_out():
-    # two chunks per warp: the one-call build takes the cooperative kernel with its grid barriers
-    w = wl.Workload("edge", 40007, 3, 40, 5, 16, 16)
+    # sixteen chunks per warp: the one-call build takes the cooperative kernel with its grid barriers
+    w = wl.Workload("edge", 330001, 3, 40, 5, 16, 16)
     inp = wl.make(w, 1)
     idx = inp["topk_idx"]
     cap = wl.worst_case_rows(w)
