@@ -50,35 +50,41 @@ DEFAULT_WORKLOAD = "roundtrip"      # the largest workload that fits one GPU
 # one metric pass) of each HBM-bound kernel, by workload, tied to the sources
 # it was measured on: a kernel whose sources changed since reports null.  How
 # each figure was taken is in profiles/traffic_by_kernel_and_workload.md.
+HOW = "ncu, one metric pass (dram__bytes_read.sum + dram__bytes_write.sum), full size, bench.py --profile, caches flushed before the kernel (ncu default); mean of two launches"
 TRAFFIC = {
     "permute_dyn_kernel": {
         "sources": ["counting_sort_bucketization_gb300/csrc/permute_kernel.cu",
                     "counting_sort_bucketization_gb300/csrc/ptx.cuh",
                     "counting_sort_bucketization_gb300/csrc/common.cuh"],
-        "sha256": None,
-        "bytes_per_launch": {},
+        "sha256": "1fffee62edae026b5ca95720bf44f6a7005c57c475b74538e2986c35734c6757",
+        "bytes_per_launch": {"roundtrip": {"bytes": 9273815552, "how": HOW}, "decode": {"bytes": 704104576, "how": HOW}, "skewed": {"bytes": 2075054464, "how": HOW}, "prefill_fp8": {"bytes": 2239759872, "how": HOW}, "prefill_fp8/sf-col-major": {"bytes": 2169645440, "how": HOW}, "decode/non-expand": {"bytes": 306171264, "how": HOW}},
     },
-    "combine_kernel": {
+    "combine": {   # combine_bulk_kernel (round-trip, skewed) or combine_kernel (decode), by batch size
         "sources": ["counting_sort_bucketization_gb300/csrc/combine_kernel.cu",
                     "counting_sort_bucketization_gb300/csrc/ptx.cuh",
                     "counting_sort_bucketization_gb300/csrc/common.cuh"],
-        "sha256": None,
-        "bytes_per_launch": {},
+        "sha256": "1d7fa4833fe27b2beefab776118bdb1ed1ec0cc4cff3b374cb607c376180c629",
+        "bytes_per_launch": {"roundtrip": {"bytes": 9192805888, "how": HOW}, "skewed": {"bytes": 1876997632, "how": HOW}, "decode": {"bytes": 477020928, "how": HOW}},
     },
     "sf_col_major_kernel": {
         "sources": ["counting_sort_bucketization_gb300/csrc/sf_layout_kernel.cu",
                     "counting_sort_bucketization_gb300/csrc/ptx.cuh",
                     "counting_sort_bucketization_gb300/csrc/common.cuh"],
-        "sha256": None,
-        "bytes_per_launch": {},
+        "sha256": "efff3440144641a56f852de8f68d122acfa0cf96531f3c0882b1463378b547f9",
+        "bytes_per_launch": {"prefill_fp8/sf-col-major": {"bytes": 11648640, "how": HOW}},
     },
 }
 
 # Kernels behind each stage of a step (the layout's depend on the batch size).
 STAGE_KERNEL = {"permute": "permute_dyn_kernel", "permute_ranks": "permute_dyn_kernel",
-                "combine": "combine_kernel", "sf_col_major": "sf_col_major_kernel",
+                "combine": "combine_bulk_kernel or combine_kernel", "sf_col_major": "sf_col_major_kernel",
                 "layout": "count_tiles + scan_columns + rank_maps, or layout_fused_kernel",
                 "rank_rows": "rank_rows_kernel"}
+STAGE_TRAFFIC = {"permute": "permute_dyn_kernel", "permute_ranks": "permute_dyn_kernel", "combine": "combine",
+                 "sf_col_major": "sf_col_major_kernel"}
+# Batches of at least this many tokens per resident CTA of the bulk combine
+# (3 per SM) take that kernel; smaller ones the register kernel.
+COMBINE_BULK_MIN_TOKENS_PER_CTA, COMBINE_BULK_CTAS_PER_SM = 12, 3
 HBM_STAGES = ("permute", "permute_ranks", "combine", "sf_col_major")
 
 # The other large workloads, each with a short clocked loop of its own in the
@@ -545,12 +551,20 @@ def time_case(case: Case, steps: int, warmup: int, flush: Flusher, world: int, s
             "host_enqueue_steps": n_enq}
 
 
+def kernel_of(case: Case, stage: str) -> str:
+    if stage != "combine":
+        return STAGE_KERNEL[stage]
+    sms = torch.cuda.get_device_properties(case.dev).multi_processor_count
+    bulk = case.w.num_tokens >= COMBINE_BULK_MIN_TOKENS_PER_CTA * COMBINE_BULK_CTAS_PER_SM * sms
+    return "combine_bulk_kernel" if bulk else "combine_kernel"
+
+
 def roofline_of(case: Case, stage: str, kern_ms: dict, peak: dict) -> dict:
-    kernel = STAGE_KERNEL[stage]
+    kernel = kernel_of(case, stage)
     t_s = kern_ms[stage] / 1e3
     ab = case.ab[stage]
     achieved = ab / t_s / 1e9
-    traffic, how = traffic_of(kernel, case.key)
+    traffic, how = traffic_of(STAGE_TRAFFIC[stage], case.key)
     r = {"kernel": kernel, "bound": "hbm", "achieved": achieved, "peak": peak["hbm_gbs"],
          "peak_source": peak["source"], "unit": "GB/s", "frac": achieved / peak["hbm_gbs"], "traffic": traffic,
          "traffic_source": how, "algorithmic_bytes_per_launch": ab, "launch_ms": kern_ms[stage]}
