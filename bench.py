@@ -247,11 +247,31 @@ class ClockSampler:
                                           "-lms", "100", "-i", str(self._index)],
                                          stdout=self._file, stderr=subprocess.DEVNULL)
             self._smi_t0 = time.perf_counter()
+            self._smi_lines = 0
             self.source = "nvidia-smi every 100 ms"
             time.sleep(0.3)
         except OSError:
             self._smi = None
         return self
+
+    def _read_smi(self):
+        """nvidia-smi's complete lines so far (one every 100 ms from its start) as samples."""
+        bits = (0x8, 0x40, 0x20, 0x4)
+        with open(self._file.name) as f:
+            lines = f.readlines()
+        for i in range(self._smi_lines, len(lines)):
+            if not lines[i].endswith("\n"):
+                break
+            self._smi_lines = i + 1
+            parts = [p.strip() for p in lines[i].split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                mask = sum(b for b, fl in zip(bits, parts[3:7]) if fl == "Active")
+                self.samples.append((self._smi_t0 + i * 0.1, float(parts[0]), float(parts[1]), mask,
+                                     float(parts[2])))
+            except ValueError:
+                continue
 
     def stop(self):
         self._stop.set()
@@ -263,25 +283,23 @@ class ClockSampler:
                 self._smi.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self._smi.kill()
-            bits = (0x8, 0x40, 0x20, 0x4)
-            dt = 0.1
-            with open(self._file.name) as f:
-                for i, line in enumerate(f):
-                    parts = [p.strip() for p in line.split(",")]
-                    if len(parts) < 7:
-                        continue
-                    try:
-                        mask = sum(b for b, fl in zip(bits, parts[3:7]) if fl == "Active")
-                        self.samples.append((self._smi_t0 + i * dt, float(parts[0]), float(parts[1]), mask,
-                                             float(parts[2])))
-                    except ValueError:
-                        continue
+            self._read_smi()
             os.unlink(self._file.name)
             self._smi = None
 
     def window(self, t0: float, t1: float) -> dict | None:
+        """Samples taken between t0 and t1; for a region shorter than the sampling
+        period, the first sample after t0 (waiting up to a few periods for it)."""
         if self.source is None:
             return None
+        period = 0.1 if self._smi is not None else self.period
+        deadline = time.perf_counter() + 4 * period + 0.05
+        while True:
+            if self._smi is not None:
+                self._read_smi()
+            if any(s[0] >= t0 for s in self.samples) or time.perf_counter() > deadline:
+                break
+            time.sleep(period / 2)
         inside = [s for s in self.samples if t0 <= s[0] <= t1]
         if not inside:   # a window shorter than the period: the first sample after its start
             after = [s for s in self.samples if s[0] >= t0]
@@ -652,7 +670,10 @@ def run_e2e(case: Case, args, world: int, dev) -> dict:
         (sf_h.numel() * 4 if sf_h is not None else 0)
     d2h = outs_h[0].numel() * outs_h[0].element_size()
     chunk_of = lambda n_chunks: -(-N // max(1, n_chunks))
-    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    # Its own step count (not --steps): filling and draining the batches in
+    # flight costs about one step's worth of one-way link time, so a few dozen
+    # steps keep that a few per cent of the measurement.
+    e2e_steps = max(3, args.e2e_steps)
     eo = case.eo
     expert = (lambda lay_, recv_, recv_sf_: eo) if do_combine else None
     sf_cols = case.sf_d.shape[1] if case.sf_d is not None else 0
@@ -878,8 +899,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", choices=list(wl.WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--tokens", type=int, default=None,
                     help="tokens per batch instead of the workload's (same recipe); for small profiling cases")
-    ap.add_argument("--e2e-steps", type=int, default=200,
-                    help="timed end-to-end steps (enough that filling and draining the batches in flight is ~1 %%)")
+    ap.add_argument("--e2e-steps", type=int, default=60,
+                    help="timed end-to-end steps (filling and draining the batches in flight is ~1 step of them)")
     ap.add_argument("--e2e-chunks", type=int, default=1, help="token chunks the host copies are split into")
     ap.add_argument("--e2e-lanes", type=int, default=3, help="batches in flight in the end-to-end leg")
     ap.add_argument("--no-e2e", action="store_true", help="leave out the end-to-end leg")

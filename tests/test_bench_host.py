@@ -86,3 +86,30 @@ def test_reference_arm_other_ranks_exit_without_work(capsys, monkeypatch):
     monkeypatch.setenv("WORLD_SIZE", "2")
     bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "0"])
     assert capsys.readouterr().out.strip() == ""
+
+
+def test_clock_window_summarises_only_its_region_and_waits_for_a_short_one():
+    """The clock record of a timed region: the samples taken inside it, their
+    median, maximum and throttle reasons; a region shorter than the sampling
+    period gets the first sample after its start, which the summary waits for."""
+    import threading
+    import time
+
+    cs = bench.ClockSampler(0)
+    cs.source, cs.period = "synthetic", 0.005
+    t = time.perf_counter()
+    cs.samples = [(t - 2.0, 1500.0, 2070.0, 0x0, 100.0),          # before: not counted
+                  (t - 1.0, 2070.0, 2070.0, 0x4, 900.0),          # inside [t-1.5, t-0.5]
+                  (t - 0.9, 2000.0, 2070.0, 0x8 | 0x20, 950.0)]   # inside, two slowdown reasons
+    w = cs.window(t - 1.5, t - 0.5)
+    assert w["samples"] == 2 and w["sm_mhz"] == 2035.0 and w["sm_max_mhz"] == 2070.0 and w["sm_mhz_min"] == 2000.0
+    assert w["reasons"] == ["hw_slowdown", "sw_power_cap", "sw_thermal_slowdown"] and w["power_w_max"] == 950.0
+
+    def late():
+        time.sleep(0.01)
+        cs.samples.append((time.perf_counter(), 2070.0, 2070.0, 0x0, 400.0))
+
+    threading.Thread(target=late).start()
+    t0 = time.perf_counter()
+    w = cs.window(t0, t0 + 0.001)          # ends before any sample: waits for the next one
+    assert w["samples"] == 1 and w["sm_mhz"] == 2070.0 and w["reasons"] == []

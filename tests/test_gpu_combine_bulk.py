@@ -78,3 +78,39 @@ def test_bulk_combine_skips_and_reports_slots_past_the_rows():
     dst[dst >= keep] = -1
     ref = oracle.combine(bf16_bits(eo), dst, inp["weights"].numpy())
     check_combine(bf16_bits(out), ref)
+
+
+def test_roundtrip_whole_rows_and_combine():
+    """The round-trip workload at full size (131072 tokens, hidden 4096), in the
+    launch configuration bench.py times: every receive row and every combined
+    token compared with the oracle's, bit for bit.  The oracle runs its own
+    layout, permute and stand-in expert on the host (about 17 GB of host memory)."""
+    from test_gpu_parity import scale_rows_on_gpu, u8
+
+    w = wl.WORKLOADS["roundtrip"]
+    inp = wl.make(w)
+    cap = wl.worst_case_rows(w)
+    N, K, H = w.num_tokens, w.topk, w.hidden
+    ref = oracle.layout(inp["topk_idx"].numpy(), w.num_experts, w.num_ranks, w.alignment, capacity_rows=cap)
+    rows = ref["total_rows"]
+    _, ref_recv, _ = oracle.permute(u8(inp["x"]), ref["dst_slot"], ref["expert_offset"], ref["expert_count"], rows)
+    ref_eo = oracle.expert_scale(ref_recv.view(np.uint16).reshape(rows, H), ref["expert_offset"],
+                                 inp["expert_scale"].numpy())
+    ref_out = oracle.combine(ref_eo, ref["dst_slot"], inp["weights"].numpy())
+
+    lay = binding.Layout(w, cap, device=DEV).build(inp["topk_idx"].to(DEV))
+    recv = torch.empty((cap, H), dtype=torch.bfloat16, device=DEV)
+    lay.permute(inp["x"].to(DEV), recv)
+    eo = scale_rows_on_gpu(recv, lay.expert_offset, inp["expert_scale"], rows)
+    out = torch.empty((N, H), dtype=torch.bfloat16, device=DEV)
+    lay.combine(eo, inp["weights"].to(DEV), out)
+    assert lay.error() == 0
+    np.testing.assert_array_equal(lay.dst_slot.cpu().numpy().reshape(N, K), ref["dst_slot"])
+    step = 1 << 16
+    for lo in range(0, rows, step):
+        hi = min(rows, lo + step)
+        np.testing.assert_array_equal(u8(recv[lo:hi]), ref_recv[lo:hi], err_msg=f"receive rows {lo}..{hi}")
+    del recv, eo
+    for lo in range(0, N, step):
+        hi = min(N, lo + step)
+        check_combine(bf16_bits(out[lo:hi]), ref_out[lo:hi])
