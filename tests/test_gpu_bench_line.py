@@ -44,6 +44,8 @@ def test_native_line_keeps_the_contract():
     assert isinstance(d["gpu_launches"], int) and d["gpu_launches"] >= 5 * 3
     assert "clocks" in d
     assert e2e["link_ceiling_tokens_per_s"] > 0 and 0 < e2e["frac_of_link"]
+    assert len(e2e["trials"]) == 3 and e2e["steps"] == 5
+    assert sorted(t["tokens_per_s"] for t in e2e["trials"])[1] == pytest.approx(e2e["value"])
     assert _number(d["host_enqueue_us_per_step"]) and d["host_enqueue_us_per_step"] > 0
     assert set(d["rooflines"]) == {"permute", "combine"}
     for r in d["rooflines"].values():
