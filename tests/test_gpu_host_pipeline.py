@@ -123,6 +123,25 @@ def test_pipelined_batches(name, chunk, lanes):
         np.testing.assert_array_equal(o.view(torch.int16).numpy().view(np.uint16), oracle_batch(b, w))
 
 
+@pytest.mark.parametrize("chunk", [0, 6000])
+def test_pipelined_batches_through_the_bulk_combine(chunk):
+    # round-trip routing, 12000 tokens per batch (and 6000-token chunks): every
+    # combine launch is large enough for the bulk-copy combine kernel
+    w = wl.WORKLOADS["roundtrip"].replace(num_tokens=12000, hidden=512)
+    cap = wl.worst_case_rows(w)
+    pipe = binding.HostPipeline(w, cap, w.hidden, lanes=3, chunk_tokens=chunk, device=DEV)
+    expert = stand_in_expert(wl.expert_scale(w).to(DEV))
+    batches = [wl.make(w, 40 + b) for b in range(4)]
+    host = [(b["topk_idx"].pin_memory(), b["x"].pin_memory(), b["weights"].pin_memory()) for b in batches]
+    outs = [torch.full((w.num_tokens, w.hidden), 5.0, dtype=torch.bfloat16).pin_memory() for _ in batches]
+    done = [pipe.submit(i, x, wt, o, expert) for (i, x, wt), o in zip(host, outs)]
+    for ev in done:
+        ev.synchronize()
+    assert pipe.errors() == [0] * 3
+    for b, o in zip(batches, outs):
+        np.testing.assert_array_equal(o.view(torch.int16).numpy().view(np.uint16), oracle_batch(b, w))
+
+
 def test_pipelined_dispatch_only_fp8():
     # expert=None: the receive rows come back to host memory; fp8 rows with scale factors
     w = wl.WORKLOADS["prefill_fp8"].replace(num_tokens=2000)
