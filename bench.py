@@ -732,6 +732,47 @@ def run_e2e(case: Case, args, world: int, dev) -> dict:
             else "HostPipeline: moe_dispatch_from_host + receive rows copied back"}
 
 
+def run_graph(case: Case, steps: int, warmup: int, flush: Flusher, world: int) -> dict:
+    """The same step captured once as a CUDA graph (binding.StepGraph) and
+    replayed: device time per step (events around each replay, L2 flushed
+    before it) and the host's time to enqueue one replay."""
+    from counting_sort_bucketization_gb300 import binding
+    dev = case.dev
+    eo = case.eo
+    g = binding.StepGraph(case.w, case.cap, case.w.hidden, expert=(lambda lay, recv, sf: eo) if case.do_combine
+                          else None, x_dtype=case.x_d.dtype, device=dev)
+    g.topk_idx.copy_(case.idx_d)
+    g.x.copy_(case.x_d)
+    g.weights.copy_(case.wt_d)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        flush()
+        g.replay()
+    evs = [new_events(2) for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        flush()
+        evs[i][0].record(stream)
+        g.replay()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    n = max(1, min(steps, 50))
+    h0 = time.perf_counter()
+    for _ in range(n):
+        g.replay()
+    h1 = time.perf_counter()
+    torch.cuda.synchronize(dev)
+    assert g.error() == 0, "device error in the graph replays"
+    ms = reduce_max(float(np.mean([e[0].elapsed_time(e[1]) for e in evs])), world, dev)
+    res = {"ms_per_step": ms, "tokens_per_s": world * case.w.num_tokens / (ms / 1e3), "steps": steps,
+           "host_us_per_replay": (h1 - h0) / n * 1e6,
+           "note": "the step's kernels (and the stand-in expert's, if any) captured once with binding.StepGraph "
+                   "and replayed; host_us_per_replay is the wall time of enqueueing one replay"}
+    del g
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_layout_only(args, local):
     """Time the layout step alone (ids in, maps out): small on the device at any
     workload size, so it is also the command to profile the layout kernels with."""
@@ -791,6 +832,9 @@ def run_native(args, rank, world, local):
     e2e_line = None
     if not args.non_expand and not profile and not args.no_e2e:
         e2e_line = run_e2e(case, args, world, dev)
+    graph_line = None
+    if not args.non_expand and case.sf_d is None and not profile and not args.no_graph:
+        graph_line = run_graph(case, args.steps, args.warmup, flush, world)
     line = {
         "metric": METRIC, "value": summ["tokens_per_s"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t["ms_per_step"], "higher_is_better": True, "scaling": "weak",
@@ -811,6 +855,7 @@ def run_native(args, rank, world, local):
         "dispatch_tokens_per_s": summ["dispatch_tokens_per_s"],
         "layout": summ["layout"],
         "host_enqueue_us_per_step": t["host_enqueue_us_per_step"],
+        "graph": graph_line,
         "host_enqueue_note": f"wall time of {t['host_enqueue_steps']} steps' calls (Python binding + C ABI + "
                             "launches) enqueued back to back, divided by the steps; no synchronisation inside",
         "e2e": e2e_line,
@@ -922,6 +967,7 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-trials", type=int, default=3, help="end-to-end trials; the line reports the median")
     ap.add_argument("--e2e-lanes", type=int, default=3, help="batches in flight in the end-to-end leg")
     ap.add_argument("--no-e2e", action="store_true", help="leave out the end-to-end leg")
+    ap.add_argument("--no-graph", action="store_true", help="leave out the CUDA-graph replay of the step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-max-passes", type=int, default=20)
     ap.add_argument("--ref-seconds", type=float, default=75.0)

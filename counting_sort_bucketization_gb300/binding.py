@@ -562,6 +562,59 @@ class HostPipeline:
         return [lane["layout"].error(lane["stream"]) for lane in self._lanes]
 
 
+class StepGraph:
+    """One dispatch -> expert -> combine step captured once as a CUDA graph and
+    replayed, for serving loops where launching the step's kernels one by one
+    from the host costs as much as running them.
+
+    The step's device tensors are fixed at capture: copy each batch into
+    ``topk_idx`` [N, K], ``x`` [N, H] and ``weights`` [N, K] (owned by this
+    object), call ``replay()``, and read ``recv_x`` (the receive buffer) and
+    ``out`` (the combined tokens).  ``expert(layout, recv_x, None)`` is captured
+    with the step and must return the bf16 expert outputs in receive-row order;
+    with ``expert=None`` the step is a dispatch only.  The library's kernels go
+    into the graph with their programmatic-dependent-launch edges, and the
+    step is run once outside capture first so that every one-time host lookup
+    (shared-memory limits, occupancies) is done before it.  ``error()`` reads
+    and clears the device error word (it synchronises; call it between replays).
+    """
+
+    def __init__(self, desc, capacity_rows: int, hidden: int, expert=None, x_dtype=torch.bfloat16, device="cuda"):
+        N, K = int(desc.num_tokens), int(desc.topk)
+        self.device = torch.device(device)
+        self.layout = Layout(desc, capacity_rows, device=self.device)
+        self.topk_idx = torch.full((N, K), -1, dtype=torch.int64, device=self.device)
+        self.x = torch.zeros((N, hidden), dtype=x_dtype, device=self.device)
+        self.weights = torch.zeros((N, K), dtype=torch.float32, device=self.device)
+        self.recv_x = torch.empty((int(capacity_rows), hidden), dtype=x_dtype, device=self.device)
+        self.out = torch.empty((N, hidden), dtype=torch.bfloat16, device=self.device) if expert is not None else None
+        self._expert = expert
+
+        side = torch.cuda.Stream(self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(side):
+            self._step()
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        torch.cuda.synchronize(self.device)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self._step()
+
+    def _step(self):
+        self.layout.build(self.topk_idx)
+        self.layout.permute(self.x, self.recv_x)
+        if self._expert is not None:
+            eo = self._expert(self.layout, self.recv_x, None)
+            self.layout.combine(eo, self.weights, self.out)
+
+    def replay(self) -> None:
+        """Run the captured step on the current stream."""
+        self.graph.replay()
+
+    def error(self) -> int:
+        return self.layout.error()
+
+
 def dispatch(topk_idx, x, num_experts, num_ranks, alignment, sf=None, capacity_rows=None, stream=None):
     """Count, scan and permute in one call; returns ``(layout, recv_x, recv_sf)``.
 

@@ -47,6 +47,8 @@ def test_native_line_keeps_the_contract():
     assert len(e2e["trials"]) == 3 and e2e["steps"] == 5
     assert sorted(t["tokens_per_s"] for t in e2e["trials"])[1] == pytest.approx(e2e["value"])
     assert _number(d["host_enqueue_us_per_step"]) and d["host_enqueue_us_per_step"] > 0
+    gr = d["graph"]
+    assert gr["steps"] == 5 and gr["ms_per_step"] > 0 and gr["host_us_per_replay"] > 0
     assert set(d["rooflines"]) == {"permute", "combine"}
     for r in d["rooflines"].values():
         assert r["bound"] == "hbm" and abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
