@@ -48,8 +48,9 @@ DEFAULT_WORKLOAD = "roundtrip"      # the largest workload that fits one GPU
 
 # DRAM traffic per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum,
 # one metric pass) of each HBM-bound kernel, by workload, tied to the sources
-# it was measured on: a kernel whose sources changed since reports null.  How
-# each figure was taken is in profiles/traffic_by_kernel_and_workload.md.
+# it was measured on: a kernel whose sources changed since reports null.  The
+# captures ran `bench.py --profile` at full size, caches flushed before each
+# captured kernel (ncu's default); each figure is the mean of two launches.
 HOW = "ncu, one metric pass (dram__bytes_read.sum + dram__bytes_write.sum), full size, bench.py --profile, caches flushed before the kernel (ncu default); mean of two launches"
 TRAFFIC = {
     "permute_dyn_kernel": {
