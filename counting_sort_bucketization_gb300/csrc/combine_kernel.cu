@@ -10,10 +10,15 @@
 // from 0, ascending k, one fused multiply-add per term, one bf16 rounding) is
 // the plain definition and makes the result bit-reproducible.
 //
-// HBM-bound: each thread owns 16-byte column vectors of the row and issues
-// the loads of up to 8 expert rows before any arithmetic, so 8 x 16 B per
-// thread are in flight; slots and weights of the CTA's token block are staged
-// in shared memory once.
+// HBM-bound.  Two kernels, chosen by batch size:
+//  - combine_bulk_kernel (from 12 tokens per resident CTA): a persistent
+//    grid whose producer warps move each token's expert rows into a shared-
+//    memory ring with bulk copies while consumer warps run the fma chain out
+//    of shared memory (its own section below);
+//  - combine_kernel (smaller batches): each thread owns 16-byte column
+//    vectors of the row and issues the loads of up to 8 expert rows before any
+//    arithmetic, so 8 x 16 B per thread are in flight; slots and weights of the
+//    CTA's token block are staged in shared memory once.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -157,8 +162,9 @@ __global__ void __launch_bounds__(kCombineThreads)
 }
 
 // ------------------------------------------------------ bulk-copy combine
-// The default path.  A persistent grid; in each CTA one producer warp
-// claims tokens from a counter in the workspace (two claims ahead) and
+// Batches of 12 or more tokens per resident CTA.  A persistent grid; in each
+// CTA one producer warp takes tokens (its first two fixed, the rest claimed
+// from a counter in the workspace, three tokens in flight) and
 // moves the token's expert rows, a piece of the row at a time, into a ring of
 // shared-memory stages with bulk copies (cp.async.bulk, completion on the
 // stage's mbarrier): lane k copies row k, so the K copies of a piece go out
