@@ -64,8 +64,8 @@ TRAFFIC = {
         "sources": ["counting_sort_bucketization_gb300/csrc/combine_kernel.cu",
                     "counting_sort_bucketization_gb300/csrc/ptx.cuh",
                     "counting_sort_bucketization_gb300/csrc/common.cuh"],
-        "sha256": "1d7fa4833fe27b2beefab776118bdb1ed1ec0cc4cff3b374cb607c376180c629",
-        "bytes_per_launch": {"roundtrip": {"bytes": 9192805888, "how": HOW}, "skewed": {"bytes": 1876997632, "how": HOW}, "decode": {"bytes": 477020928, "how": HOW}},
+        "sha256": "088673f399f2a3677b81538aed54aeb2aa922f9fefa85e7585eeec034566d335",
+        "bytes_per_launch": {"roundtrip": {"bytes": 9192338560, "how": HOW}, "skewed": {"bytes": 1876517888, "how": HOW}, "decode": {"bytes": 477036800, "how": HOW}},
     },
     "sf_col_major_kernel": {
         "sources": ["counting_sort_bucketization_gb300/csrc/sf_layout_kernel.cu",
