@@ -69,10 +69,12 @@ def test_prefill_fp8_full_size(fused):
     np.testing.assert_array_equal(got, want)
 
 
-@pytest.mark.parametrize("name,cols", [("tiny", 1), ("tiny", 3), ("tiny", 64), ("tiny", 65), ("tiny", 130),
-                                       ("decode", 56), ("skewed", 7)])
+@pytest.mark.parametrize("name,cols", [("tiny", 1), ("tiny", 3), ("tiny", 4), ("tiny", 64), ("tiny", 65),
+                                       ("tiny", 130), ("tiny", 132), ("decode", 56), ("decode", 128),
+                                       ("skewed", 7), ("skewed", 20)])
 def test_workload_columns(name, cols):
-    # column counts below, at and above one 64-column pass through the tile
+    # column counts below, at and above one 64-column pass through the tile,
+    # with 16-byte row loads (a multiple of 4 words) and with single words
     err, got, want, _, _ = expand_case(wl.WORKLOADS[name], wl.SEEDS[name], cols=cols)
     assert err == 0
     np.testing.assert_array_equal(got, want)
