@@ -603,6 +603,7 @@ def case_summary(case: Case, t: dict, peak: dict, world: int) -> dict:
     return {
         "config": config_of(case.w), "ms_per_step": t["ms_per_step"], "tokens_per_s": world * N / (t["ms_per_step"] / 1e3),
         "dispatch_tokens_per_s": world * N / (dispatch_ms / 1e3),
+        **({"combine_tokens_per_s": world * N / (kern["combine"] / 1e3)} if "combine" in kern else {}),
         "kernels_ms": kern, "kernels_gbs": {s: rl[s]["achieved"] for s in hbm},
         "kernels_frac": {s: rl[s]["frac"] for s in hbm},
         "kernels_frac_dram": {s: rl[s].get("frac_dram") for s in hbm},
@@ -854,6 +855,7 @@ def run_native(args, rank, world, local):
                               "events keep each kernel from starting during the previous one's tail, so their "
                               "sum can exceed ms_per_step, which is timed per whole step"},
         "dispatch_tokens_per_s": summ["dispatch_tokens_per_s"],
+        **({"combine_tokens_per_s": summ["combine_tokens_per_s"]} if "combine_tokens_per_s" in summ else {}),
         "layout": summ["layout"],
         "host_enqueue_us_per_step": t["host_enqueue_us_per_step"],
         "graph": graph_line,

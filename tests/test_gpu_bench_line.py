@@ -50,6 +50,9 @@ def test_native_line_keeps_the_contract():
     gr = d["graph"]
     assert gr["steps"] == 5 and gr["ms_per_step"] > 0 and gr["host_us_per_replay"] > 0
     assert set(d["rooflines"]) == {"permute", "combine"}
+    N = d["config"]["num_tokens"]
+    assert d["combine_tokens_per_s"] == pytest.approx(N / (d["kernels_ms"]["combine"] / 1e3))
+    assert d["dispatch_tokens_per_s"] == pytest.approx(N / ((d["kernels_ms"]["layout"] + d["kernels_ms"]["permute"]) / 1e3))
     for r in d["rooflines"].values():
         assert r["bound"] == "hbm" and abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
     clk = d["clocks"]
