@@ -590,6 +590,14 @@ def roofline_of(case: Case, stage: str, kern_ms: dict, peak: dict) -> dict:
     if traffic is not None:
         r["achieved_dram"] = traffic / t_s / 1e9
         r["frac_dram"] = r["achieved_dram"] / peak["hbm_gbs"]
+    if stage == "sf_col_major":
+        r["note"] = ("its data stays in L2: each token's scale row comes from DRAM once and then from L2 for "
+                     "every further slot, and the column writes are still in L2 when it ends; the kernel moves "
+                     f"{2 * case.ab['rows'] * case.w.sf_row_bytes / 1e6:.1f} MB through L2 (gathered reads + column "
+                     "writes), so neither fraction measures it against its own bound")
+    elif stage == "combine":
+        r["note"] = ("the combine starts while the permute's last writes (up to ~60 MB) are still dirty in L2, and "
+                     "their write-back runs during it; traffic, captured with caches flushed, leaves that out")
     return r
 
 
