@@ -622,20 +622,33 @@ def case_summary(case: Case, t: dict, peak: dict, world: int) -> dict:
     }
 
 
-def link_ceiling(h2d, d2h, reps: int, dev) -> dict:
+def step_gaps(ends_ms) -> dict:
+    """Steady state and stalls of a loop from the completion time of each step
+    (ms from the loop's start): the median step, the mean, and the steps that
+    took more than twice the median."""
+    gaps = [b - a for a, b in zip([0.0] + ends_ms[:-1], ends_ms)][1:]   # the first step includes the ramp
+    med = float(np.median(gaps))
+    return {"median_ms": med, "mean_ms": float(np.mean(gaps)),
+            "stalls_ms": [round(g, 1) for g in gaps if g > 2 * med]}
+
+
+def link_ceiling(h2d, d2h, reps: int, dev, steps: int) -> dict:
     """Pinned host<->device copies of exactly one step's bytes: each direction
-    alone, then both at once on two streams (the ceiling of any pipeline that
-    moves these bytes).  ``h2d`` is a list of (device dst, host src), ``d2h`` of
-    (host dst, device src)."""
+    alone (``reps`` steps), then both at once on two streams for ``steps``
+    steps, as many as an end-to-end trial, with an event after each (the
+    ceiling of any pipeline that moves these bytes, measured over as long a
+    stretch as the trial, so that the link's own stalls count in both).
+    ``h2d`` is a list of (device dst, host src), ``d2h`` of (host dst, device src)."""
     main = torch.cuda.current_stream(dev)
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-    def timed(directions):
-        # Each repetition forks the directions onto their streams and joins them again.
+    def timed(directions, n):
+        # Each step forks the directions onto their streams and joins them again.
         torch.cuda.synchronize(dev)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a = torch.cuda.Event(enable_timing=True)
+        ends = new_events(n)
         a.record(main)
-        for _ in range(reps):
+        for i in range(n):
             for s, pairs in directions:
                 s.wait_stream(main)
                 with torch.cuda.stream(s):
@@ -643,18 +656,21 @@ def link_ceiling(h2d, d2h, reps: int, dev) -> dict:
                         dst.copy_(src, non_blocking=True)
             for s, _ in directions:
                 main.wait_stream(s)
-        b.record(main)
+            ends[i].record(main)
         torch.cuda.synchronize(dev)
-        return a.elapsed_time(b) / reps / 1e3   # s per step
+        t = [a.elapsed_time(e) for e in ends]
+        return t[-1] / n / 1e3, t   # s per step, completion times (ms)
 
     bi = sum(d.numel() * d.element_size() for d, _ in h2d)
     bo = sum(d.numel() * d.element_size() for d, _ in d2h)
-    timed([(s_in, h2d), (s_out, d2h)])   # warm-up
-    t_in = timed([(s_in, h2d)])
-    t_out = timed([(s_out, d2h)])
-    t_both = timed([(s_in, h2d), (s_out, d2h)])
+    timed([(s_in, h2d), (s_out, d2h)], reps)   # warm-up
+    t_in, _ = timed([(s_in, h2d)], reps)
+    t_out, _ = timed([(s_out, d2h)], reps)
+    t_both, ends = timed([(s_in, h2d), (s_out, d2h)], steps)
+    g = step_gaps(ends)
     return {"h2d_gbs": bi / t_in / 1e9, "d2h_gbs": bo / t_out / 1e9, "both_gbs": (bi + bo) / t_both / 1e9,
-            "step_ms_both_directions": t_both * 1e3, "reps": reps}
+            "step_ms_both_directions": t_both * 1e3, "steady_step_ms_both_directions": g["median_ms"],
+            "stalls_ms": g["stalls_ms"], "reps_one_direction": reps, "steps_both_directions": steps}
 
 
 def run_e2e(case: Case, args, world: int, dev) -> dict:
@@ -704,14 +720,18 @@ def run_e2e(case: Case, args, world: int, dev) -> dict:
         out = []
         for _ in range(n_trials):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ends = new_events(e2e_steps)
             a.record(stream)
             for i in range(e2e_steps):
-                pipe.submit(idx_h, x_h, wt_h, outs_h[i % n_lanes], expert, sf_h)
+                li = pipe.next_lane
+                pipe.submit(idx_h, x_h, wt_h, outs_h[li], expert, sf_h)
+                ends[i].record(pipe.lane(li)["stream"])   # batch i's result is in host memory
             pipe.join(stream)
             b.record(stream)
             torch.cuda.synchronize(dev)
-            link = link_ceiling(h2d_pairs, [(outs_h[0], d2h_src)], 5, dev) if with_link else None
-            out.append((a.elapsed_time(b) / e2e_steps, link))
+            gaps = step_gaps([a.elapsed_time(e) for e in ends])
+            link = link_ceiling(h2d_pairs, [(outs_h[0], d2h_src)], 5, dev, e2e_steps) if with_link else None
+            out.append((a.elapsed_time(b) / e2e_steps, link, gaps))
         assert pipe.errors() == [0] * n_lanes, "device error in the end-to-end steps"
         del pipe
         torch.cuda.empty_cache()
@@ -723,7 +743,7 @@ def run_e2e(case: Case, args, world: int, dev) -> dict:
     # reports the median trial and every trial with its ceiling.
     trials = trials_ms(lanes, args.e2e_chunks, max(1, args.e2e_trials), True)
     order = sorted(range(len(trials)), key=lambda i: trials[i][0])
-    med_ms, link = trials[order[len(order) // 2]]
+    med_ms, link, _ = trials[order[len(order) // 2]]
     step_ms = reduce_max(med_ms, world, dev)
     # One batch in flight, its copies overlapped with the kernels in 4 chunks: the reference point.
     one_ms = reduce_max(trials_ms(1, 4, 1, False)[0][0], world, dev)
@@ -734,10 +754,15 @@ def run_e2e(case: Case, args, world: int, dev) -> dict:
             "value_one_batch_in_flight_4_chunks": world * N / (one_ms / 1e3),
             "link": link, "link_ceiling_tokens_per_s": ceiling, "frac_of_link": value / ceiling,
             "trials": [{"tokens_per_s": world * N / (ms / 1e3), "link_both_gbs": lk["both_gbs"],
-                        "frac_of_link": (N / (ms / 1e3)) / (N / (lk["step_ms_both_directions"] / 1e3))}
-                       for ms, lk in trials],
+                        "frac_of_link": lk["step_ms_both_directions"] / ms,
+                        "steady_step_ms": gp["median_ms"], "stalls_ms": gp["stalls_ms"],
+                        "link_steady_step_ms": lk["steady_step_ms_both_directions"],
+                        "link_stalls_ms": lk["stalls_ms"]}
+                       for ms, lk, gp in trials],
             "note": f"median of {len(trials)} trials of {e2e_steps} steps; link and ceiling from the link "
-                    "measurement right after that trial",
+                    f"measurement right after that trial: {e2e_steps} steps of the same bytes in both directions "
+                    "with no kernels, so that stalls of the host link (steps over twice the median) weigh on "
+                    "both alike; steady_step_ms is a trial's median step",
             "api": "HostPipeline: moe_dispatch_from_host + moe_combine_to_host" if do_combine
             else "HostPipeline: moe_dispatch_from_host + receive rows copied back"}
 

@@ -524,6 +524,11 @@ class HostPipeline:
     def lane(self, i: int) -> dict:
         return self._lanes[i]
 
+    @property
+    def next_lane(self) -> int:
+        """Index of the lane the next ``submit`` uses."""
+        return self._next
+
     def submit(self, topk_idx_host, x_host, weights_host, out_host, expert, sf_host=None) -> torch.cuda.Event:
         lane = self._lanes[self._next]
         self._next = (self._next + 1) % len(self._lanes)

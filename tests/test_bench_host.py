@@ -113,3 +113,13 @@ def test_clock_window_summarises_only_its_region_and_waits_for_a_short_one():
     t0 = time.perf_counter()
     w = cs.window(t0, t0 + 0.001)          # ends before any sample: waits for the next one
     assert w["samples"] == 1 and w["sm_mhz"] == 2070.0 and w["reasons"] == []
+
+
+def test_step_gaps_steady_state_and_stalls():
+    # completion times of a loop: 6.3 ms steps with one 34.1 ms stall; the
+    # first step (ramp) is left out of the statistics
+    g = bench.step_gaps([7.0, 13.3, 19.6, 25.9, 60.0, 66.3, 72.6])
+    assert g["median_ms"] == pytest.approx(6.3)
+    assert g["mean_ms"] == pytest.approx((72.6 - 7.0) / 6)
+    assert g["stalls_ms"] == [34.1]
+    assert bench.step_gaps([1.0, 2.0, 3.0])["stalls_ms"] == []

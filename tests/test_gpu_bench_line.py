@@ -46,6 +46,10 @@ def test_native_line_keeps_the_contract():
     assert e2e["link_ceiling_tokens_per_s"] > 0 and 0 < e2e["frac_of_link"]
     assert len(e2e["trials"]) == 3 and e2e["steps"] == 5
     assert sorted(t["tokens_per_s"] for t in e2e["trials"])[1] == pytest.approx(e2e["value"])
+    for t in e2e["trials"]:
+        assert t["steady_step_ms"] > 0 and t["link_steady_step_ms"] > 0
+        assert isinstance(t["stalls_ms"], list) and isinstance(t["link_stalls_ms"], list)
+    assert e2e["link"]["steps_both_directions"] == 5 and e2e["link"]["steady_step_ms_both_directions"] > 0
     assert _number(d["host_enqueue_us_per_step"]) and d["host_enqueue_us_per_step"] > 0
     gr = d["graph"]
     assert gr["steps"] == 5 and gr["ms_per_step"] > 0 and gr["host_us_per_replay"] > 0
