@@ -1000,7 +1000,7 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=60,
                     help="timed end-to-end steps (filling and draining the batches in flight is ~1 step of them)")
     ap.add_argument("--e2e-chunks", type=int, default=1, help="token chunks the host copies are split into")
-    ap.add_argument("--e2e-trials", type=int, default=3, help="end-to-end trials; the line reports the median")
+    ap.add_argument("--e2e-trials", type=int, default=5, help="end-to-end trials; the line reports the median")
     ap.add_argument("--e2e-lanes", type=int, default=3, help="batches in flight in the end-to-end leg")
     ap.add_argument("--no-e2e", action="store_true", help="leave out the end-to-end leg")
     ap.add_argument("--no-graph", action="store_true", help="leave out the CUDA-graph replay of the step")

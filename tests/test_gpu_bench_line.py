@@ -20,8 +20,8 @@ def _number(v):
 
 def test_native_line_keeps_the_contract():
     proc = subprocess.run([sys.executable, os.path.join(REPO, "bench.py"), "--workload", "decode", "--steps", "5",
-                           "--warmup", "3", "--e2e-steps", "5", "--breakdown-steps", "5", "--cpu-seconds", "1",
-                           "--cpu-max-passes", "1", "--per-config-only", "decode/non-expand",
+                           "--warmup", "3", "--e2e-steps", "5", "--e2e-trials", "3", "--breakdown-steps", "5",
+                           "--cpu-seconds", "1", "--cpu-max-passes", "1", "--per-config-only", "decode/non-expand",
                            "--per-config-steps", "20"],
                           cwd=REPO, capture_output=True, text=True, timeout=600)
     assert proc.returncode == 0, proc.stderr[-3000:]
